@@ -1,0 +1,444 @@
+#!/usr/bin/env python3
+"""Benchmark of the collective datapath on one GB300 (or N independent replicas).
+
+One step = one AllReduce (sum) over 8 emulated ranks of 32 Mi bf16 elements
+(64 MiB) each, through the library's C ABI: layout, tiling, one persistent
+kernel running the N-to-1 reduce Atom, written to all 8 outputs.  The metric
+is HBM GB/s counted as algorithmic bytes (every input byte read once, every
+output byte written once: 2 * 8 * 64 MiB = 1 GiB per step) over device time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl own|reference]
+
+Prints one JSON line (rank 0).  With --impl reference the CPU oracle is timed
+on the host cores on a bounded sample of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORLD = 8
+N_ELEMS = 32 << 20          # per rank
+ELEM = 2                    # bf16
+S = N_ELEMS * ELEM          # bytes per rank
+ALGO_BYTES = 2 * WORLD * S  # N inputs read + N outputs written
+METRIC = "AllReduce/ReduceScatter/AllGather/AllToAll HBM GB/s vs size, % of GB300 HBM peak"
+WORKLOAD = "AllReduce sum, 8 emulated ranks on one GPU, bf16 in/out, fp32 ascending-rank accumulation, " \
+           "32 Mi elements (64 MiB) per rank, N(0,1), seed 1"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["own", "reference"], default="own")
+    ap.add_argument("--no-extras", action="store_true", help="skip the per-collective side table")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------ distributed
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float, device=None) -> float:
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed work runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- helpers
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "collective_datapath_reduce_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the AllReduce kernel from the committed ncu summary,
+    or None when the kernel sources changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "allreduce_bf16_8x64MiB.traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("src_hash") != source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------- own arm
+
+def run_own(args, dist):
+    import torch
+    from collective_datapath_reduce_gb300 import _build, inputs
+    from collective_datapath_reduce_gb300 import purlin as P
+
+    _build.build()
+    P.load()
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    dist.init("nccl")
+    stream = torch.cuda.Stream(device=dev)
+
+    x = inputs.w2_allreduce_bf16(WORLD, N_ELEMS, seed=1)          # host, (8, 32 Mi) bf16 bits
+    host_in = [torch.from_numpy(x[r].view(np.int16)).pin_memory() for r in range(WORLD)]
+    src = [torch.empty(N_ELEMS, dtype=torch.int16, device=dev) for _ in range(WORLD)]
+    dst = [torch.empty(N_ELEMS, dtype=torch.int16, device=dev) for _ in range(WORLD)]
+    host_out = [torch.empty(N_ELEMS, dtype=torch.int16).pin_memory() for _ in range(WORLD)]
+    with torch.cuda.stream(stream):
+        for r in range(WORLD):
+            src[r].copy_(host_in[r], non_blocking=True)
+    stream.synchronize()
+
+    st, h = P.purlin_initialize(WORLD, None, 0, stream)
+    P.check(st, "purlin_initialize")
+    sptr = [t.data_ptr() for t in src]
+    dptr = [t.data_ptr() for t in dst]
+
+    def step():
+        st = P.purlin_all_reduce(h, sptr, dptr, S, P.PL_BF16, P.PL_DETERMINISTIC, stream)
+        if st != P.PL_OK:
+            raise P.PurlinError(st, "purlin_all_reduce")
+
+    for _ in range(args.warmup):
+        step()
+    stream.synchronize()
+    _, tune = P.purlin_tune_get(h, P.PL_COLL_ALL_REDUCE, P.PL_BF16, S)
+
+    clocks = ClockSampler(dist.local)
+    clocks.start()
+    time.sleep(0.3)
+    K = args.steps
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(K):
+        ev0[i].record(stream)
+        step()
+        ev1[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ev0, ev1))
+    time.sleep(0.1)
+    clk = clocks.stop()
+    st, dev_status = P.purlin_status_get(h, stream)
+    P.check(st, "purlin_status_get")
+    if dev_status:
+        raise P.PurlinError(dev_status, "device")
+
+    total_ms = dist.max(total_ms, dev)
+    ms_per_step = total_ms / K
+    value = dist.world * ALGO_BYTES * K / (total_ms / 1e3) / 1e9
+
+    # end to end: host buffers in, result back to host, every step
+    Ke = max(3, min(K, 20))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(Ke):
+            for r in range(WORLD):
+                src[r].copy_(host_in[r], non_blocking=True)
+            step()
+            for r in range(WORLD):
+                host_out[r].copy_(dst[r], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    e2e_ms = dist.max(e0.elapsed_time(e1), dev) / Ke
+    e2e = {"value": round(dist.world * ALGO_BYTES / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": WORLD * S, "d2h_bytes_per_step": WORLD * S, "ms_per_step": round(e2e_ms, 4)}
+
+    peak, peak_kind = measured_peaks()
+    achieved = ALGO_BYTES / (kernel_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(),
+                "peak_source": f"hbm_gbs of {peak_kind}", "kernel_ms": round(kernel_ms, 5),
+                "algorithmic_bytes_per_launch": ALGO_BYTES}
+
+    extras = None
+    if not args.no_extras and dist.rank == 0:
+        extras = side_table(P, h, stream, dev)
+
+    P.check(P.purlin_finalize(h, stream), "purlin_finalize")
+
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(x, budget_s=12.0)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "world": WORLD, "bytes_per_rank": S,
+                   "algorithmic_bytes_per_step": ALGO_BYTES,
+                   "parallelism": f"replicas{dist.world}" if dist.world > 1 else "single-gpu",
+                   "l2": "inputs 512 MiB and outputs 512 MiB per step exceed the 126 MiB L2; no flush",
+                   "tune": tune},
+        "roofline": roofline, "e2e": e2e, "gpu_launches": K, "clocks": clk,
+        "cpu_baseline": cpu,
+        "pct_of_hbm_peak": round(100 * value / dist.world / peak, 2),
+    }
+    if extras:
+        line["collectives"] = extras
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+def side_table(P, h, stream, dev):
+    """A few more points of the metric (GB/s by collective and size) and the
+    device-to-device memcpy ceiling, each a short event-timed loop."""
+    import torch
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    out = {}
+
+    def timeit(fn, iters=20):
+        for _ in range(3):
+            fn()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for _ in range(iters):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / iters
+
+    def bufs(n, count, dtype=torch.uint8):
+        if dtype == torch.uint8:
+            return [torch.randint(0, 256, (n,), dtype=torch.uint8, device=dev, generator=gen) for _ in range(count)]
+        return [torch.randn(n, dtype=dtype, device=dev, generator=gen) for _ in range(count)]
+
+    def gbps(nbytes, ms):
+        return round(nbytes / (ms / 1e3) / 1e9, 1)
+
+    with torch.cuda.stream(stream):
+        for mib in (64, 256):
+            n = mib << 20
+            a, b = bufs(n, 1)[0], torch.empty(n, dtype=torch.uint8, device=dev)
+            ms = timeit(lambda: b.copy_(a))
+            out[f"d2d_memcpy_{mib}MiB"] = {"GB/s": gbps(2 * n, ms), "us": round(ms * 1e3, 2)}
+            del a, b
+        # ReduceScatter fp32, 8 x 256 MiB -> 8 x 32 MiB
+        n = 64 << 20
+        src = bufs(n, WORLD, torch.float32)
+        dstb = [torch.empty(n // WORLD, dtype=torch.float32, device=dev) for _ in range(WORLD)]
+        ms = timeit(lambda: P.check(P.purlin_reduce_scatter(h, src, dstb, n * 4, P.PL_F32, 0, stream)))
+        out["reduce_scatter_f32_8x256MiB"] = {"GB/s": gbps(WORLD * n * 4 + n * 4, ms), "us": round(ms * 1e3, 1)}
+        del src, dstb
+        # AllReduce two-shot layout at the headline size
+        srcb = bufs(N_ELEMS, WORLD, torch.bfloat16)
+        dstb = [torch.empty_like(t) for t in srcb]
+        P.check(P.purlin_tune_override(h, {"layout": P.PL_LAYOUT_TWO_SHOT}))
+        ms = timeit(lambda: P.check(P.purlin_all_reduce(h, srcb, dstb, S, P.PL_BF16, 0, stream)))
+        out["all_reduce_two_shot_bf16_8x64MiB"] = {"GB/s": gbps(ALGO_BYTES, ms), "us": round(ms * 1e3, 1)}
+        P.check(P.purlin_tune_override(h, None))
+        del srcb, dstb
+        # AllGather / AllToAll u8 at 1 KiB, 1 MiB, 64 MiB per rank
+        for size in (1 << 10, 1 << 20, 64 << 20):
+            src = bufs(size, WORLD)
+            dag = [torch.empty(WORLD * size, dtype=torch.uint8, device=dev) for _ in range(WORLD)]
+            ms = timeit(lambda: P.check(P.purlin_all_gather(h, src, dag, size, stream)))
+            out[f"all_gather_u8_8x{size >> 10}KiB"] = {"GB/s": gbps(WORLD * size * (1 + WORLD), ms),
+                                                       "us": round(ms * 1e3, 2)}
+            del dag
+            da = [torch.empty(size, dtype=torch.uint8, device=dev) for _ in range(WORLD)]
+            ms = timeit(lambda: P.check(P.purlin_all_to_all(h, src, da, size, stream)))
+            out[f"all_to_all_u8_8x{size >> 10}KiB"] = {"GB/s": gbps(2 * WORLD * size, ms), "us": round(ms * 1e3, 2)}
+            del src, da
+        torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------- CPU baseline
+
+def _oracle_sample(x, n_sample):
+    import oracle
+    ins = [x[r, :n_sample] for r in range(x.shape[0])]
+    t0 = time.perf_counter()
+    oracle.all_reduce(ins, "bf16")
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(x, budget_s=12.0):
+    """The CPU oracle, as it stands, on a bounded sample of the workload."""
+    n = 1 << 20
+    t = _oracle_sample(x, n)
+    n_sample = int(min(x.shape[1], max(n, n * (budget_s / 4) / max(t, 1e-3))))
+    n_sample -= n_sample % 8
+    reps, spent = 0, 0.0
+    while spent < budget_s and reps < 50:
+        spent += _oracle_sample(x, n_sample)
+        reps += 1
+    per = spent / reps
+    nbytes = 2 * x.shape[0] * n_sample * ELEM
+    return {"value": round(nbytes / per / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {n_sample} of {x.shape[1]} elements of each of the {x.shape[0]} ranks, "
+                      f"{reps} runs, {per:.3f} s each (numpy, single-threaded)"}
+
+
+# ----------------------------------------------------------- reference arm
+
+def run_reference(args, dist):
+    """The oracle times itself on the host cores; rank 0 only."""
+    if dist.rank != 0:
+        return
+    from collective_datapath_reduce_gb300 import inputs
+    n_total = N_ELEMS
+    x = inputs.w2_allreduce_bf16(WORLD, n_total, seed=1)
+    t = _oracle_sample(x, 1 << 20)
+    steps = args.steps + args.warmup
+    per_step_budget = max(0.05, 120.0 / max(steps, 1))
+    n_sample = int(min(n_total, max(1 << 16, (1 << 20) * per_step_budget / max(t, 1e-4))))
+    n_sample -= n_sample % 8
+    for _ in range(args.warmup):
+        _oracle_sample(x, n_sample)
+    times = [_oracle_sample(x, n_sample) for _ in range(args.steps)]
+    per = sum(times) / len(times)
+    nbytes = 2 * WORLD * n_sample * ELEM
+    value = round(nbytes / per / 1e9, 4)
+    sample = f"first {n_sample} of {n_total} elements of each of the {WORLD} ranks per step (numpy, single-threaded)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "world": WORLD, "bytes_per_rank": S, "sampled_elements_per_rank": n_sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }), flush=True)
+
+
+def main():
+    args = parse()
+    dist = Dist()
+    if args.impl == "reference":
+        run_reference(args, dist)
+        return
+    run_own(args, dist)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,39 @@
+// Kernel arguments of one collective launch, shared by the host runtime and
+// the device code.  Passed by value as a __grid_constant__ parameter: the
+// per-rank buffer pointers live in the kernel's parameter space, so a plan
+// (offsets only) serves any buffers with the same alignment.
+#pragma once
+
+#include <stdint.h>
+
+#include "plan.h"
+
+namespace pl {
+
+// Control words at the start of the workspace.
+enum : int { kCtlStatus = 0, kCtlEpoch = 1, kCtlDone = 2 };
+constexpr int kCtlBytes = 256;   // flags start here
+constexpr int kDevTimeout = 7;   // PL_ERR_TIMEOUT
+
+struct KArgs {
+  const char* in[kMaxWorld];
+  char* out[kMaxWorld];
+  const Item* items;
+  const uint32_t* cta_begin;  // contiguous assignment (nullptr when strided)
+  uint32_t n_items;
+  uint32_t strided;           // item i on CTA i % grid; also marks plans with flags
+  uint32_t* flags;
+  uint32_t* ctl;              // status, epoch, done counter
+  unsigned long long timeout_ns;
+  uint32_t drop_notify;       // 1 + item whose notify is skipped, or 0
+  int nsrc;                   // sources of each reduce item
+  int store_hint;             // 1 write-back, 2 streaming
+};
+
+// Kernel entry points (device function addresses), by variant.  nullptr when
+// the variant is not built.
+const void* kernel_copy(int unroll);
+const void* kernel_reduce_f32(int nsrc, int unroll);
+const void* kernel_reduce_bf16(int nsrc, int unroll);
+
+}  // namespace pl

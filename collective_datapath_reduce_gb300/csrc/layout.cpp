@@ -1,0 +1,475 @@
+// Layout engine and tiling (host only).
+//
+// Step 1, layouts: each collective becomes a list of pieces (see plan.h).
+//   AllReduce, one-shot  (Iris docs, "Device Context", all_reduce_one_shot:
+//       every rank reads all ranks and reduces locally): one reduce piece over
+//       the whole buffer, sources = all inputs, destinations = all outputs.
+//   AllReduce, two-shot  (same page, all_reduce_two_shot: each rank reduces
+//       only its share, then the result is scattered, with ready flags):
+//       rank o owns the o-th of world near-equal element ranges; per tile t of
+//       that range a reduce piece writes out[o] and raises flag (o, t), and a
+//       copy piece waits on the flag and copies out[o] to every other output.
+//   ReduceScatter  (NKI, reduce_scatter_hbm_kernel): piece r reduces chunk r of
+//       all inputs into out[r].
+//   AllGather      (NKI, all_gather_hbm_kernel): piece s copies in[s] to offset
+//       s*S of every output (one read, world writes).
+//   AllToAll       (NKI, all_to_all_hbm_kernel): piece (s, d) copies chunk d of
+//       in[s] to chunk s of out[d].
+//   V variants     (Purlin README summary): the same pieces at prefix-sum
+//       displacements of the given byte counts.
+// Step 2, tiling: pieces are concatenated into one byte space that is cut
+// into `grid` contiguous, equal shares (Iris docs, reduce_scatter:
+// contiguous work distribution), one per persistent CTA.  Plans with SNAC
+// flags keep each piece whole and deal the items out round-robin instead, so
+// that producers and consumers of a flag run at about the same time.
+#include "plan.h"
+
+#include <algorithm>
+#include <cstring>
+#include <sstream>
+
+#include "purlin_gb.h"
+
+namespace pl {
+
+namespace {
+
+struct Piece {
+  uint64_t src_off, dst_off, len;
+  uint32_t src_mask, dst_mask;
+  uint32_t wait, notify;
+};
+
+constexpr uint64_t kMaxItemBytes = 1ull << 30;
+
+inline uint32_t all_ranks(int world) { return (world >= 32) ? 0xFFFFFFFFu : ((1u << world) - 1u); }
+inline uint64_t ceil_div(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+inline int popcount32(uint32_t x) { return __builtin_popcount(x); }
+
+bool is_reduce_coll(int coll) {
+  return coll == kAllReduce || coll == kReduceScatter || coll == kReduceScatterV ||
+         coll == kAtomReduce;
+}
+
+// Split a piece whose destinations do not all share one address residue
+// modulo 16 into one piece per residue class (the Atoms store one vector to
+// every destination of an item and need them co-aligned).
+void push_grouped(std::vector<Piece>& out, const Piece& p, const uint8_t* dst_res) {
+  if (p.len == 0) return;
+  uint32_t left = p.dst_mask;
+  while (left) {
+    int first = __builtin_ctz(left);
+    uint32_t res = (dst_res[first] + p.dst_off) & 15u;
+    uint32_t group = 0;
+    for (uint32_t m = left; m; m &= m - 1) {
+      int r = __builtin_ctz(m);
+      if (((dst_res[r] + p.dst_off) & 15u) == res) group |= 1u << r;
+    }
+    Piece q = p;
+    q.dst_mask = group;
+    out.push_back(q);
+    left &= ~group;
+  }
+}
+
+}  // namespace
+
+int elem_size(int dtype) { return dtype == kF32 ? 4 : (dtype == kBF16 ? 2 : 1); }
+
+size_t n_sizes(int coll, int world) {
+  switch (coll) {
+    case kAllGatherV:
+    case kReduceScatterV:
+      return (size_t)world;
+    case kAllToAllV:
+      return (size_t)world * (size_t)world;
+    case kAtomReduce:
+      return 3;
+    default:
+      return 1;
+  }
+}
+
+// Initial tuning table.  Entries are replaced by the measured sweep; the
+// defaults are what a streaming kernel on 148+ SMs usually wants: two
+// 512-thread CTAs per SM, enough 16-byte loads in flight per thread to cover
+// HBM latency, and no shrinking of the grid until a CTA would get less than
+// 32 KiB of work.
+Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
+  (void)dtype;
+  (void)bytes_per_rank;
+  Tune t;
+  const bool red = is_reduce_coll(coll);
+  t.layout = kOneShot;
+  t.path = kPathRegister;
+  t.threads = 512;
+  t.ctas_per_sm = 2;
+  t.unroll = red ? (world <= 4 ? 2 : 1) : 4;
+  t.chunk_bytes = 64 * 1024;
+  t.stages = 4;
+  t.store_hint = 1;
+  t.min_cta_bytes = 32 * 1024;
+  return t;
+}
+
+Tune tune_merge(const Tune& b, const Tune& o) {
+  Tune t = b;
+  if (o.layout) t.layout = o.layout;
+  if (o.ctas_per_sm) t.ctas_per_sm = o.ctas_per_sm;
+  if (o.threads) t.threads = o.threads;
+  if (o.unroll) t.unroll = o.unroll;
+  if (o.path) t.path = o.path;
+  if (o.chunk_bytes) t.chunk_bytes = o.chunk_bytes;
+  if (o.stages) t.stages = o.stages;
+  if (o.store_hint) t.store_hint = o.store_hint;
+  if (o.min_cta_bytes) t.min_cta_bytes = o.min_cta_bytes;
+  return t;
+}
+
+static int validate_tune(const Tune& t) {
+  if (t.layout < kOneShot || t.layout > kTwoShot) return PL_ERR_UNSUPPORTED;
+  if (t.threads < 64 || t.threads > 512 || t.threads % 32) return PL_ERR_INVALID_ARG;
+  if (t.ctas_per_sm < 1 || t.ctas_per_sm > 32) return PL_ERR_INVALID_ARG;
+  if (t.unroll < 1 || t.unroll > 8) return PL_ERR_INVALID_ARG;
+  if (t.path != kPathRegister && t.path != kPathBulk) return PL_ERR_UNSUPPORTED;
+  if (t.chunk_bytes < 1024 || t.chunk_bytes > (64 << 20) || t.chunk_bytes % 16) return PL_ERR_INVALID_ARG;
+  if (t.stages < 2 || t.stages > 8) return PL_ERR_INVALID_ARG;
+  if (t.store_hint < 1 || t.store_hint > 2) return PL_ERR_INVALID_ARG;
+  if (t.min_cta_bytes < 16) return PL_ERR_INVALID_ARG;
+  return PL_OK;
+}
+
+int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsizes,
+               const uint8_t* src_res, const uint8_t* dst_res, int sm_count, int max_ctas_per_sm,
+               const Tune& tune_in, Plan* out) {
+  if (!out || !sizes) return PL_ERR_INVALID_ARG;
+  if (world < 1 || world > kMaxWorld) return PL_ERR_INVALID_ARG;
+  if (coll < kAllReduce || coll > kAtomReduce) return PL_ERR_UNSUPPORTED;
+  if (dtype < kU8 || dtype > kBF16) return PL_ERR_UNSUPPORTED;
+  if (sm_count < 1) return PL_ERR_INVALID_ARG;
+  if (nsizes != n_sizes(coll, world)) return PL_ERR_INVALID_ARG;
+  const bool red = is_reduce_coll(coll);
+  if (red && dtype == kU8) return PL_ERR_UNSUPPORTED;
+
+  uint8_t zeros[kMaxWorld] = {};
+  if (!src_res) src_res = zeros;
+  if (!dst_res) dst_res = zeros;
+
+  Plan p;
+  p.coll = coll;
+  p.world = world;
+  p.dtype = dtype;
+  p.elem = red ? elem_size(dtype) : 1;
+  const uint64_t E = (uint64_t)p.elem;
+  p.tune = tune_merge(tune_table(coll, world, dtype, sizes[0]), tune_in);
+  if (int st = validate_tune(p.tune)) return st;
+  if (max_ctas_per_sm > 0) p.tune.ctas_per_sm = std::min(p.tune.ctas_per_sm, max_ctas_per_sm);
+
+  const uint32_t ALL = all_ranks(world);
+  std::vector<Piece> pieces;
+  bool sync = false;
+  uint32_t n_flags = 0;
+
+  // ------------------------------------------------------------ layouts
+  switch (coll) {
+    case kAllReduce: {
+      const uint64_t S = sizes[0];
+      if (S % E) return PL_ERR_ALIGNMENT;
+      for (int r = 0; r < world; ++r) p.in_bytes[r] = p.out_bytes[r] = S;
+      p.work_bytes = 2ull * world * S;
+      p.reduce = true;
+      p.nsrc = world;
+      if (p.tune.layout == kTwoShot && world > 1) {
+        sync = true;
+        const uint64_t n = S / E;
+        const uint64_t T = std::max<uint64_t>(16, (uint64_t)p.tune.chunk_bytes / 16 * 16);
+        uint64_t start[kMaxWorld + 1];
+        start[0] = 0;
+        for (int o = 0; o < world; ++o)
+          start[o + 1] = start[o] + (n / world + ((uint64_t)o < n % world ? 1 : 0)) * E;
+        uint64_t tiles[kMaxWorld], tmax = 0;
+        for (int o = 0; o < world; ++o) {
+          tiles[o] = ceil_div(start[o + 1] - start[o], T);
+          tmax = std::max(tmax, tiles[o]);
+        }
+        n_flags = (uint32_t)(world * tmax);
+        uint64_t n_items = 0;
+        for (int o = 0; o < world; ++o) n_items += 2 * tiles[o];
+        const uint64_t gcap = (uint64_t)p.tune.ctas_per_sm * sm_count;
+        const uint64_t G = std::max<uint64_t>(1, std::min<uint64_t>(gcap, n_items));
+        // a copy round trails its reduce round by about one wave of CTAs
+        const uint64_t lag = std::max<uint64_t>(1, ceil_div(G, 2ull * world));
+        auto reduce_piece = [&](int o, uint64_t t) {
+          uint64_t off = start[o] + t * T, len = std::min(T, start[o + 1] - off);
+          Piece q{off, off, len, ALL, 1u << o, 0, (uint32_t)(o * tmax + t + 1)};
+          push_grouped(pieces, q, dst_res);
+        };
+        auto copy_piece = [&](int o, uint64_t t) {
+          uint64_t off = start[o] + t * T, len = std::min(T, start[o + 1] - off);
+          Piece q{off, off, len, 1u << (16 + o), ALL & ~(1u << o), (uint32_t)(o * tmax + t + 1), 0};
+          push_grouped(pieces, q, dst_res);
+        };
+        for (uint64_t t = 0; t < tmax + lag; ++t) {
+          if (t < tmax)
+            for (int o = 0; o < world; ++o)
+              if (t < tiles[o]) reduce_piece(o, t);
+          if (t >= lag && t - lag < tmax)
+            for (int o = 0; o < world; ++o)
+              if (t - lag < tiles[o]) copy_piece(o, t - lag);
+        }
+      } else {
+        p.tune.layout = kOneShot;
+        push_grouped(pieces, Piece{0, 0, S, ALL, ALL, 0, 0}, dst_res);
+      }
+      break;
+    }
+    case kReduceScatter: {
+      const uint64_t S = sizes[0];
+      if (S % E) return PL_ERR_ALIGNMENT;
+      if ((S / E) % world) return PL_ERR_INVALID_ARG;
+      const uint64_t c = S / world;
+      for (int r = 0; r < world; ++r) {
+        p.in_bytes[r] = S;
+        p.out_bytes[r] = c;
+        push_grouped(pieces, Piece{r * c, 0, c, ALL, 1u << r, 0, 0}, dst_res);
+      }
+      p.work_bytes = (uint64_t)world * S + S;
+      p.reduce = true;
+      p.nsrc = world;
+      break;
+    }
+    case kReduceScatterV: {
+      uint64_t total = 0;
+      for (int r = 0; r < world; ++r) {
+        if (sizes[r] % E) return PL_ERR_ALIGNMENT;
+        total += sizes[r];
+      }
+      uint64_t off = 0;
+      for (int r = 0; r < world; ++r) {
+        p.in_bytes[r] = total;
+        p.out_bytes[r] = sizes[r];
+        push_grouped(pieces, Piece{off, 0, sizes[r], ALL, 1u << r, 0, 0}, dst_res);
+        off += sizes[r];
+      }
+      p.work_bytes = (uint64_t)world * total + total;
+      p.reduce = true;
+      p.nsrc = world;
+      break;
+    }
+    case kAllGather: {
+      const uint64_t S = sizes[0];
+      for (int s = 0; s < world; ++s) {
+        p.in_bytes[s] = S;
+        p.out_bytes[s] = (uint64_t)world * S;
+        push_grouped(pieces, Piece{0, s * S, S, 1u << s, ALL, 0, 0}, dst_res);
+      }
+      p.work_bytes = (uint64_t)world * S + (uint64_t)world * world * S;
+      break;
+    }
+    case kAllToAll: {
+      const uint64_t S = sizes[0];
+      if (S % world) return PL_ERR_INVALID_ARG;
+      const uint64_t c = S / world;
+      for (int s = 0; s < world; ++s) p.in_bytes[s] = p.out_bytes[s] = S;
+      for (int s = 0; s < world; ++s)
+        for (int d = 0; d < world; ++d)
+          push_grouped(pieces, Piece{d * c, s * c, c, 1u << s, 1u << d, 0, 0}, dst_res);
+      p.work_bytes = 2ull * world * S;
+      break;
+    }
+    case kAllGatherV: {
+      uint64_t total = 0;
+      for (int s = 0; s < world; ++s) total += sizes[s];
+      uint64_t displ = 0;
+      for (int s = 0; s < world; ++s) {
+        p.in_bytes[s] = sizes[s];
+        p.out_bytes[s] = total;
+        push_grouped(pieces, Piece{0, displ, sizes[s], 1u << s, ALL, 0, 0}, dst_res);
+        displ += sizes[s];
+      }
+      p.work_bytes = total + (uint64_t)world * total;
+      break;
+    }
+    case kAllToAllV: {
+      uint64_t total = 0;
+      for (int s = 0; s < world; ++s) {
+        uint64_t send = 0;
+        for (int d = 0; d < world; ++d) send += sizes[s * world + d];
+        p.in_bytes[s] = send;
+        total += send;
+      }
+      for (int d = 0; d < world; ++d) {
+        uint64_t recv = 0;
+        for (int s = 0; s < world; ++s) recv += sizes[s * world + d];
+        p.out_bytes[d] = recv;
+      }
+      for (int s = 0; s < world; ++s) {
+        for (int d = 0; d < world; ++d) {
+          uint64_t sdispl = 0, rdispl = 0;
+          for (int k = 0; k < d; ++k) sdispl += sizes[s * world + k];
+          for (int k = 0; k < s; ++k) rdispl += sizes[k * world + d];
+          push_grouped(pieces, Piece{sdispl, rdispl, sizes[s * world + d], 1u << s, 1u << d, 0, 0},
+                       dst_res);
+        }
+      }
+      p.work_bytes = 2ull * total;
+      break;
+    }
+    case kAtomCopy: {
+      const uint64_t S = sizes[0];
+      p.in_bytes[0] = S;
+      for (int d = 0; d < world; ++d) p.out_bytes[d] = S;
+      push_grouped(pieces, Piece{0, 0, S, 1u, ALL, 0, 0}, dst_res);
+      p.work_bytes = S + (uint64_t)world * S;
+      break;
+    }
+    case kAtomReduce: {
+      const uint64_t S = sizes[0];
+      const uint64_t ns = sizes[1], nd = sizes[2];
+      if (ns < 1 || nd < 1 || ns > (uint64_t)world || nd > (uint64_t)world) return PL_ERR_INVALID_ARG;
+      if (S % E) return PL_ERR_ALIGNMENT;
+      for (uint64_t s = 0; s < ns; ++s) p.in_bytes[s] = S;
+      for (uint64_t d = 0; d < nd; ++d) p.out_bytes[d] = S;
+      push_grouped(pieces, Piece{0, 0, S, all_ranks((int)ns), all_ranks((int)nd), 0, 0}, dst_res);
+      p.work_bytes = (ns + nd) * S;
+      p.reduce = ns > 1;
+      p.nsrc = (int)ns;
+      break;
+    }
+  }
+  if (!p.reduce) p.nsrc = 1;
+
+  // ------------------------------------------------------------ tiling
+  const uint64_t gcap = (uint64_t)p.tune.ctas_per_sm * (uint64_t)sm_count;
+  if (sync) {
+    p.strided = true;
+    p.n_flags = (int)n_flags;
+    const uint64_t n = pieces.size();
+    p.grid = (int)std::max<uint64_t>(1, std::min<uint64_t>(gcap, n));
+    p.items.reserve(n);
+    for (const Piece& q : pieces)
+      p.items.push_back(Item{q.src_off, q.dst_off, q.len, q.src_mask, q.dst_mask, q.wait, q.notify});
+  } else {
+    uint64_t W = 0;
+    for (const Piece& q : pieces) W += q.len;
+    uint64_t G = std::max<uint64_t>(1, std::min<uint64_t>(gcap, ceil_div(W, (uint64_t)p.tune.min_cta_bytes)));
+    G = std::min<uint64_t>(G, std::max<uint64_t>(1, W / 16));
+    p.grid = (int)G;
+    std::vector<uint64_t> start(pieces.size() + 1, 0);
+    for (size_t i = 0; i < pieces.size(); ++i) start[i + 1] = start[i] + pieces[i].len;
+    // boundary b of the concatenated space -> (piece, offset rounded down to 16)
+    auto locate = [&](uint64_t b, size_t& pi, uint64_t& off) {
+      if (b >= W) {
+        pi = pieces.size();
+        off = 0;
+        return;
+      }
+      pi = (size_t)(std::upper_bound(start.begin(), start.end(), b) - start.begin()) - 1;
+      off = (b - start[pi]) & ~(uint64_t)15;
+    };
+    size_t cp = 0;
+    uint64_t co = 0;
+    p.cta_begin.push_back(0);
+    for (uint64_t c = 0; c < G; ++c) {
+      size_t ep;
+      uint64_t eo;
+      if (c + 1 == G) {
+        ep = pieces.size();
+        eo = 0;
+      } else {
+        // exact integer share boundary: floor((c+1) * W / G) without overflow
+        const uint64_t b = (uint64_t)(((unsigned __int128)(c + 1) * W) / G);
+        locate(b, ep, eo);
+      }
+      while (cp < ep || (cp == ep && co < eo)) {
+        const Piece& q = pieces[cp];
+        const uint64_t end = (cp == ep) ? eo : q.len;
+        // items stay below 1 GiB so the Atoms can count 16-byte vectors in 32 bits
+        for (uint64_t a = co; a < end; a += kMaxItemBytes) {
+          const uint64_t l = std::min<uint64_t>(kMaxItemBytes, end - a);
+          p.items.push_back(Item{q.src_off + a, q.dst_off + a, l, q.src_mask, q.dst_mask, 0, 0});
+        }
+        if (cp == ep) {
+          co = eo;
+          break;
+        }
+        ++cp;
+        co = 0;
+      }
+      p.cta_begin.push_back((uint32_t)p.items.size());
+    }
+  }
+  *out = std::move(p);
+  return PL_OK;
+}
+
+std::string check_plan(const Plan& p) {
+  std::ostringstream err;
+  const uint32_t ALL = all_ranks(p.world);
+  std::vector<int64_t> notified_at(p.n_flags, -1);
+  for (size_t i = 0; i < p.items.size(); ++i) {
+    const Item& it = p.items[i];
+    if (it.notify) {
+      if (it.notify > (uint32_t)p.n_flags) return "notify flag out of range";
+      notified_at[it.notify - 1] = (int64_t)i;
+    }
+  }
+  std::vector<std::vector<std::pair<uint64_t, uint64_t>>> written(p.world);
+  for (size_t i = 0; i < p.items.size(); ++i) {
+    const Item& it = p.items[i];
+    if (it.len == 0) return "empty item";
+    const uint32_t in_bits = it.src_mask & 0xFFFFu, out_bits = it.src_mask >> 16;
+    if ((in_bits & ~ALL) || (out_bits & ~ALL)) return "source mask outside the world";
+    if (!it.dst_mask || (it.dst_mask & ~ALL)) return "destination mask empty or outside the world";
+    const int nsrc = popcount32(it.src_mask);
+    if (nsrc < 1) return "item without a source";
+    if (nsrc > 1 && out_bits) return "a reduce reads outputs";
+    if (nsrc > 1 && ((it.src_off | it.dst_off | it.len) % (uint64_t)p.elem)) return "reduce not element aligned";
+    for (uint32_t m = in_bits; m; m &= m - 1) {
+      int r = __builtin_ctz(m);
+      if (it.src_off + it.len > p.in_bytes[r]) {
+        err << "item " << i << " reads past input " << r;
+        return err.str();
+      }
+    }
+    for (uint32_t m = out_bits; m; m &= m - 1) {
+      int r = __builtin_ctz(m);
+      if (it.src_off + it.len > p.out_bytes[r]) return "reads past an output";
+    }
+    for (uint32_t m = it.dst_mask; m; m &= m - 1) {
+      int r = __builtin_ctz(m);
+      if (it.dst_off + it.len > p.out_bytes[r]) {
+        err << "item " << i << " writes past output " << r;
+        return err.str();
+      }
+      written[r].push_back({it.dst_off, it.dst_off + it.len});
+    }
+    if (it.wait) {
+      if (it.wait > (uint32_t)p.n_flags) return "wait flag out of range";
+      const int64_t at = notified_at[it.wait - 1];
+      if (at < 0 || at >= (int64_t)i) return "wait without an earlier notify";
+    }
+  }
+  for (int r = 0; r < p.world; ++r) {
+    auto& w = written[r];
+    std::sort(w.begin(), w.end());
+    uint64_t covered = 0;
+    for (size_t k = 0; k < w.size(); ++k) {
+      if (k && w[k].first < w[k - 1].second) return "an output byte is written twice";
+      covered += w[k].second - w[k].first;
+    }
+    if (covered != p.out_bytes[r]) {
+      err << "output " << r << " covered " << covered << " of " << p.out_bytes[r];
+      return err.str();
+    }
+  }
+  if (!p.strided) {
+    if (p.cta_begin.size() != (size_t)p.grid + 1) return "cta ranges";
+    for (size_t c = 0; c + 1 < p.cta_begin.size(); ++c)
+      if (p.cta_begin[c] > p.cta_begin[c + 1]) return "cta ranges not monotone";
+    if (p.cta_begin.front() != 0 || p.cta_begin.back() != p.items.size()) return "cta ranges do not cover";
+  }
+  return "";
+}
+
+}  // namespace pl

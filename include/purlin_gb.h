@@ -1,0 +1,263 @@
+/*
+ * purlin_gb.h - C ABI of the collective datapath for one GB300 (sm_103a).
+ *
+ * What the library computes.  Purlin's collectives (Purlin README, purlin
+ * 0.6.4: summary paragraph and "Key Idea") are built from two datapath
+ * primitives, a copy and an N-to-1 reduce that sums several input buffers into
+ * one output, driven by layouts that say which bytes go where and whether they
+ * are copied or reduced, and by the Stage, Notify And Consume (SNAC) protocol.
+ * Here the `world` ranks of a collective are `world` separate buffers in the
+ * HBM of one GPU: rank r's input is src[r] and its output is dst[r].
+ *
+ * Semantics of each collective follow AWS Neuron NKI, "Collective
+ * Communication Kernels API Reference" (dim-0 definitions and the worked
+ * all-reduce example); the V variants are named in the Purlin README summary.
+ * Reductions are deterministic (Purlin README, "Reduction determinism"): every
+ * output element is the binary32 left fold, in ascending rank order starting
+ * from rank 0's value, of the ranks' elements, rounded once to the output type
+ * (bf16: nearest, ties to even).  Results are bit-identical from call to call.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers in src[] / dst[] are device pointers owned by the caller.  The
+ *     host arrays src[], dst[], bytes[] are read during the call only.
+ *   - `bytes` arguments count bytes, not elements.
+ *   - Every collective is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).  Argument errors are returned at once and
+ *     nothing is launched.  Errors found on the device (a SNAC wait that ran
+ *     out of time) are recorded in the handle's device status word and
+ *     reported by purlin_status_get().
+ *   - A call that moves zero bytes returns PL_OK without launching anything.
+ *   - Destination ranges must not overlap each other or any source range.
+ *     The one exception is in-place AllReduce, src[r] == dst[r].
+ *   - Reductions need every pointer aligned to the element size; copies take
+ *     any byte alignment.  16-byte alignment of every address is the fast path.
+ *   - Calls on one handle must be ordered (one stream, or streams the caller
+ *     orders): they share the handle's workspace.
+ *   - The first call of a given shape builds its plan (a small host
+ *     computation plus one upload); make it before capturing the stream into
+ *     a CUDA graph.
+ */
+#ifndef PURLIN_GB_H
+#define PURLIN_GB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PURLIN_MAX_WORLD 16
+
+typedef struct purlin_ctx* purlin_handle;
+typedef void* purlin_stream_t; /* a cudaStream_t */
+
+typedef enum {
+  PL_OK = 0,
+  PL_ERR_INVALID_ARG = 1,  /* null pointer, bad world, sizes that do not split, overlap */
+  PL_ERR_ALIGNMENT = 2,    /* a reduce pointer or size not aligned to the element size */
+  PL_ERR_UNSUPPORTED = 3,  /* e.g. a reduction over PL_U8, an unknown mode or layout */
+  PL_ERR_WORKSPACE = 4,    /* caller-provided workspace too small for this call */
+  PL_ERR_CUDA = 5,         /* a CUDA runtime call failed */
+  PL_ERR_LAUNCH = 6,       /* the kernel could not be launched */
+  PL_ERR_TIMEOUT = 7,      /* device: a SNAC consume wait gave up */
+  PL_ERR_FINALIZED = 8     /* the handle was finalized */
+} purlin_status;
+
+typedef enum { PL_U8 = 0, PL_F32 = 1, PL_BF16 = 2 } purlin_dtype;
+
+/* Purlin README, "Reduction determinism".  Only the deterministic mode exists
+ * here: the other mode of the pages needs a multicast fabric across GPUs. */
+typedef enum { PL_DETERMINISTIC = 0 } purlin_mode;
+
+typedef enum {
+  PL_COLL_ALL_REDUCE = 0,
+  PL_COLL_REDUCE_SCATTER = 1,
+  PL_COLL_ALL_GATHER = 2,
+  PL_COLL_ALL_TO_ALL = 3,
+  PL_COLL_ALL_GATHER_V = 4,
+  PL_COLL_ALL_TO_ALL_V = 5,
+  PL_COLL_REDUCE_SCATTER_V = 6,
+  PL_COLL_ATOM_COPY = 7,
+  PL_COLL_ATOM_REDUCE = 8
+} purlin_coll;
+
+/* AllReduce layouts (Iris docs, "Device Context", all_reduce_one_shot and
+ * all_reduce_two_shot).  One-shot: every byte range is reduced once and the
+ * sum stored to all ranks.  Two-shot: rank o reduces range o into its own
+ * output and notifies; a consumer then copies that range to every other rank. */
+typedef enum {
+  PL_LAYOUT_AUTO = 0,
+  PL_LAYOUT_ONE_SHOT = 1,
+  PL_LAYOUT_TWO_SHOT = 2
+} purlin_layout;
+
+/* Tuning of one call (the role of Purlin's host tuning policies).  A zero field
+ * means "take the tuning table's value". */
+typedef struct {
+  int layout;       /* purlin_layout; AllReduce only */
+  int ctas_per_sm;  /* persistent CTAs per SM (grid = ctas_per_sm x SMs, capped by work) */
+  int threads;      /* threads per CTA: a multiple of 32 in [64, 1024] */
+  int unroll;       /* 16-byte vectors in flight per thread per source, 1..8 */
+  int path;         /* 1 = register path, 2 = TMA bulk pipeline through shared memory */
+  int chunk_bytes;  /* TMA stage size per source, or SNAC tile size for the two-shot layout */
+  int stages;       /* TMA pipeline depth, 2..8 */
+  int store_hint;   /* 1 = default write-back stores, 2 = streaming (evict-first) stores */
+  int min_cta_bytes;/* fewest work bytes given to one CTA before the grid shrinks */
+} purlin_tune;
+
+/* One work item of a plan, as purlin_plan_describe reports it. */
+typedef struct {
+  uint64_t src_off;  /* byte offset into every source buffer the item reads */
+  uint64_t dst_off;  /* byte offset into every destination buffer it writes */
+  uint64_t len;      /* bytes */
+  uint32_t src_mask; /* bit r (r < 16): input of rank r; bit 16 + r: output of rank r.
+                        Several bits = N-to-1 reduce in ascending bit order. */
+  uint32_t dst_mask; /* bit r: output of rank r */
+  uint32_t wait;     /* 0, or 1 + index of the SNAC flag consumed before the item */
+  uint32_t notify;   /* 0, or 1 + index of the SNAC flag raised after the item */
+  uint32_t cta;      /* CTA that runs the item */
+  uint32_t order;    /* position of the item in that CTA's sequence */
+} purlin_item;
+
+/* ---------------------------------------------------------------- set-up */
+
+/* Bytes of workspace a handle needs for collectives of up to
+ * `max_bytes_per_rank` per rank (the SNAC signal flags plus a status word).
+ * Role of the pages' workspace of staging and signal buffers (purlin 0.6.5,
+ * "Host-side").  Returns 0 for a world outside [1, PURLIN_MAX_WORLD]. */
+size_t purlin_workspace_bytes(int world, size_t max_bytes_per_rank);
+
+/* Create a handle for `world` ranks on the current CUDA device (purlin 0.6.5,
+ * "Host-side": create once, reuse for every collective).  `workspace` is
+ * device memory owned by the caller, of `workspace_bytes` bytes, 256-byte
+ * aligned; pass NULL to let the library allocate and grow its own.  The
+ * workspace is zeroed on `stream` before the call returns.  On success *out
+ * holds the handle. */
+purlin_status purlin_initialize(int world, void* workspace, size_t workspace_bytes,
+                                purlin_stream_t stream, purlin_handle* out);
+
+/* Free what the library allocated for the handle, after work queued on
+ * `stream` is done (purlin 0.6.5, "Host-side": finalize after the last
+ * collective).  Returns the first device error still pending, if any. */
+purlin_status purlin_finalize(purlin_handle h, purlin_stream_t stream);
+
+/* ----------------------------------------------------------- collectives */
+
+/* AllReduce (NKI all_reduce_hbm_kernel: sum tensors across ranks): dst[r][i] =
+ * sum over s of src[s][i] for every r.  bytes_per_rank = size of each input
+ * and each output.  dtype PL_F32 or PL_BF16.  In-place (src[r] == dst[r]) is
+ * allowed. */
+purlin_status purlin_all_reduce(purlin_handle h, const void* const* src, void* const* dst,
+                                size_t bytes_per_rank, purlin_dtype dtype, purlin_mode mode,
+                                purlin_stream_t stream);
+
+/* ReduceScatter (NKI reduce_scatter_hbm_kernel: sum, then dim 0 is split into
+ * world chunks): dst[r][j] = sum over s of src[s][r*c + j], c = elements per
+ * chunk.  in_bytes_per_rank must split into world chunks of whole elements;
+ * each output holds in_bytes_per_rank / world bytes. */
+purlin_status purlin_reduce_scatter(purlin_handle h, const void* const* src, void* const* dst,
+                                    size_t in_bytes_per_rank, purlin_dtype dtype, purlin_mode mode,
+                                    purlin_stream_t stream);
+
+/* AllGather (NKI all_gather_hbm_kernel: gather along dim 0): dst[r] = src[0] ||
+ * src[1] || ... || src[world-1] for every r.  in_bytes_per_rank is the size of
+ * each input; each output holds world * in_bytes_per_rank bytes. */
+purlin_status purlin_all_gather(purlin_handle h, const void* const* src, void* const* dst,
+                                size_t in_bytes_per_rank, purlin_stream_t stream);
+
+/* AllToAll (NKI all_to_all_hbm_kernel: rank i receives chunk i of every
+ * input): dst[d][s*c .. s*c+c) = src[s][d*c .. d*c+c), c = bytes_per_rank /
+ * world.  bytes_per_rank (each input and each output) must split into world
+ * equal chunks. */
+purlin_status purlin_all_to_all(purlin_handle h, const void* const* src, void* const* dst,
+                                size_t bytes_per_rank, purlin_stream_t stream);
+
+/* AllGatherV (Purlin README: variable-length AllGather): dst[r] = the first
+ * bytes[0] bytes of src[0] || ... || the first bytes[world-1] bytes of
+ * src[world-1], packed in rank order, for every r.  bytes has world entries. */
+purlin_status purlin_all_gather_v(purlin_handle h, const void* const* src, void* const* dst,
+                                  const size_t* bytes, purlin_stream_t stream);
+
+/* AllToAllV (Purlin README: variable-length AllToAll).  bytes[s*world + d]
+ * bytes go from rank s to rank d.  Rank s sends its block for d from offset
+ * sum_{d'<d} bytes[s*world+d']; rank d stores the block from s at offset
+ * sum_{s'<s} bytes[s'*world+d]. */
+purlin_status purlin_all_to_all_v(purlin_handle h, const void* const* src, void* const* dst,
+                                  const size_t* bytes, purlin_stream_t stream);
+
+/* ReduceScatterV (Purlin README: variable-length ReduceScatter).  Every input
+ * holds sum_r bytes[r] bytes; dst[r] receives bytes[r] bytes, the sum over s
+ * of src[s] from offset sum_{r'<r} bytes[r'].  Each bytes[r] must be a whole
+ * number of elements. */
+purlin_status purlin_reduce_scatter_v(purlin_handle h, const void* const* src, void* const* dst,
+                                      const size_t* bytes, purlin_dtype dtype, purlin_mode mode,
+                                      purlin_stream_t stream);
+
+/* ----------------------------------------------------------------- Atoms */
+
+/* Copy Atom (purlin 0.6.5, "Samples": threads of a CTA copy one slice; src
+ * and dst may be anywhere in device memory): dst[d][0..bytes) =
+ * src[0..bytes) for each of the ndst destinations, spread over the grid. */
+purlin_status purlin_atom_copy(purlin_handle h, const void* src, void* const* dst, int ndst,
+                               size_t bytes, purlin_stream_t stream);
+
+/* N-to-1 reduce Atom (Purlin README: combines several input buffers into one
+ * output): dst[d][i] = sum over s < nsrc of src[s][i] (ascending fold) for each
+ * of the ndst destinations.  bytes = size of each buffer. */
+purlin_status purlin_atom_reduce(purlin_handle h, const void* const* src, int nsrc,
+                                 void* const* dst, int ndst, size_t bytes, purlin_dtype dtype,
+                                 purlin_stream_t stream);
+
+/* ------------------------------------------------------ status and tuning */
+
+/* Wait for `stream`'s queued work, then report (and clear) the first error
+ * recorded on the device since the last call: *device_status = PL_OK or
+ * PL_ERR_TIMEOUT.  Returns PL_OK when the query itself worked. */
+purlin_status purlin_status_get(purlin_handle h, purlin_stream_t stream, int* device_status);
+
+const char* purlin_status_string(purlin_status s);
+
+/* The tuning the handle would use for a call (table entry, then override). */
+purlin_status purlin_tune_get(purlin_handle h, purlin_coll coll, purlin_dtype dtype,
+                              size_t bytes_per_rank, purlin_tune* out);
+
+/* Override the tuning table for every later call on the handle (non-zero
+ * fields win); NULL restores the table.  Used by the tuning sweep. */
+purlin_status purlin_tune_override(purlin_handle h, const purlin_tune* t);
+
+/* Time limit of every SNAC consume wait, in nanoseconds (default 2e9). */
+purlin_status purlin_set_wait_timeout_ns(purlin_handle h, uint64_t ns);
+
+/* Test hook: the next launch on the handle skips the notify of its item with
+ * index `item` (plan order), so the consumer of that flag runs out of time and
+ * the device status reads PL_ERR_TIMEOUT.  -1 clears. */
+purlin_status purlin_debug_drop_notify(purlin_handle h, long long item);
+
+/* Device facts the handle uses: SM count, compute capability (major*10+minor),
+ * and the largest number of CTAs of the reduce kernel resident per SM. */
+purlin_status purlin_query(purlin_handle h, int* sm_count, int* arch, int* max_ctas_per_sm);
+
+/* ------------------------------------------------------- host-only plans */
+
+/* The plan a call would run, computed on the host with no GPU: the layout
+ * (pieces of copy / reduce work, Purlin README "Key Idea": layouts describe
+ * the collective) split into per-CTA work items.  `sizes` is the size
+ * argument of the collective: one value (bytes per rank) for AllReduce,
+ * ReduceScatter, AllGather, AllToAll; `world` values for AllGatherV and
+ * ReduceScatterV; world*world values for AllToAllV.  `src_addr` / `dst_addr`
+ * (world entries each, may be NULL = all 256-byte aligned) supply the buffer
+ * addresses whose low bits decide alignment.  `tune` may be NULL (table).
+ * Writes up to `cap` items; *n_items receives the total, *grid the CTA count,
+ * *n_flags the SNAC flags used. */
+purlin_status purlin_plan_describe(purlin_coll coll, int world, purlin_dtype dtype,
+                                   const size_t* sizes, const uint64_t* src_addr,
+                                   const uint64_t* dst_addr, int sm_count,
+                                   const purlin_tune* tune, purlin_item* items, size_t cap,
+                                   size_t* n_items, int* grid, int* n_flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PURLIN_GB_H */

@@ -1,0 +1,187 @@
+"""Layout engine and tiling on the CPU: plans run by the host interpreter equal the oracle.
+
+Covers every collective, worlds 1..16, sizes with ragged tails, unaligned
+V counts, buffer addresses with mixed residues modulo 16, tiny grids (many
+items per CTA) and big grids (many CTAs per piece), and both AllReduce
+layouts.  Also checks the plan's bookkeeping: CTA assignment and the SNAC
+rule that every wait follows its notify in global order.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from collective_datapath_reduce_gb300 import purlin as P
+from layout_interp import run_items
+
+RNG = np.random.default_rng(1234)
+
+
+def _describe(coll, world, dtype, sizes, sres=None, dres=None, sm=152, tune=None):
+    src_addr = [0x10000 * (r + 1) + (sres[r] if sres else 0) for r in range(world)]
+    dst_addr = [0x90000 * (r + 1) + (dres[r] if dres else 0) for r in range(world)]
+    st, items, grid, nflags = P.purlin_plan_describe(coll, world, dtype, sizes, src_addr, dst_addr, sm, tune)
+    assert st == P.PL_OK, P.purlin_status_string(st)
+    assert items or sum(sizes[:1] if coll in (0, 1, 2, 3) else sizes) == 0
+    for it in items:
+        assert 0 <= it["cta"] < grid
+    return items, grid, nflags
+
+
+def _bytes(a):
+    return np.ascontiguousarray(a).view(np.uint8).copy()
+
+
+def _draw(dtype, n):
+    if dtype == "f32":
+        return RNG.standard_normal(n).astype(np.float32)
+    return oracle.f32_to_bf16_rne(RNG.standard_normal(n).astype(np.float32))
+
+
+DT = {"f32": P.PL_F32, "bf16": P.PL_BF16}
+ESZ = {"f32": 4, "bf16": 2}
+
+
+def _res(world, aligned):
+    if aligned:
+        return [0] * world
+    return [int(x) for x in RNG.integers(0, 16, size=world)]
+
+
+TUNES = [None, {"ctas_per_sm": 1, "min_cta_bytes": 16}, {"min_cta_bytes": 1 << 20}]
+SMS = [1, 7, 152]
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 8, 16])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("layout", [P.PL_LAYOUT_ONE_SHOT, P.PL_LAYOUT_TWO_SHOT])
+def test_all_reduce_plan(world, dtype, layout):
+    E = ESZ[dtype]
+    for n in (1, 7, 1000, 4096 + 3):
+        for sm in SMS:
+            ins = [_draw(dtype, n) for _ in range(world)]
+            # element-aligned residues only (reductions need element alignment)
+            sres = [int(x) * E % 16 for x in RNG.integers(0, 16, size=world)]
+            dres = [int(x) * E % 16 for x in RNG.integers(0, 16, size=world)]
+            tune = {"layout": layout, "chunk_bytes": 1024, "ctas_per_sm": 2, "min_cta_bytes": 64}
+            items, grid, nflags = _describe(P.PL_COLL_ALL_REDUCE, world, DT[dtype], [n * E], sres, dres, sm, tune)
+            outs = [np.zeros(n * E, np.uint8) for _ in range(world)]
+            run_items(items, [_bytes(x) for x in ins], outs, dtype)
+            want = oracle.all_reduce(ins, dtype)
+            for r in range(world):
+                assert np.array_equal(outs[r], _bytes(want[r])), (n, sm, r)
+            if layout == P.PL_LAYOUT_TWO_SHOT and world > 1:
+                assert nflags > 0
+                first_notify = {}
+                for i, it in enumerate(items):
+                    if it["notify"]:
+                        first_notify[it["notify"]] = i
+                for i, it in enumerate(items):
+                    if it["wait"]:
+                        assert first_notify[it["wait"]] < i
+                        # strided: a CTA runs its items in increasing global order
+                        assert it["cta"] == i % grid
+
+
+@pytest.mark.parametrize("world", [1, 2, 5, 8])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_reduce_scatter_plans(world, dtype):
+    E = ESZ[dtype]
+    for chunk in (1, 5, 333):
+        for sm in SMS:
+            for tune in TUNES:
+                n = chunk * world
+                ins = [_draw(dtype, n) for _ in range(world)]
+                items, _, _ = _describe(P.PL_COLL_REDUCE_SCATTER, world, DT[dtype], [n * E], sm=sm, tune=tune)
+                outs = [np.zeros(chunk * E, np.uint8) for _ in range(world)]
+                run_items(items, [_bytes(x) for x in ins], outs, dtype)
+                want = oracle.reduce_scatter(ins, dtype)
+                for r in range(world):
+                    assert np.array_equal(outs[r], _bytes(want[r]))
+        # ReduceScatterV with uneven counts (some zero)
+        counts = [int(c) for c in RNG.integers(0, 40, size=world)]
+        if world > 1:
+            counts[0] = 0
+        n = sum(counts)
+        ins = [_draw(dtype, n) for _ in range(world)]
+        items, _, _ = _describe(P.PL_COLL_REDUCE_SCATTER_V, world, DT[dtype], [c * E for c in counts], sm=3,
+                                tune={"min_cta_bytes": 16})
+        outs = [np.zeros(c * E, np.uint8) for c in counts]
+        run_items(items, [_bytes(x) for x in ins], outs, dtype)
+        want = oracle.reduce_scatter_v(ins, counts, dtype)
+        for r in range(world):
+            assert np.array_equal(outs[r], _bytes(want[r]))
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 8, 16])
+@pytest.mark.parametrize("aligned", [True, False])
+def test_copy_plans(world, aligned):
+    for S in (1, 16, 1000, 4096, 65536 + 5):
+        for sm in SMS:
+            tune = TUNES[int(RNG.integers(0, len(TUNES)))]
+            sres, dres = _res(world, aligned), _res(world, aligned)
+            ins = [RNG.integers(0, 256, size=S, dtype=np.uint8) for _ in range(world)]
+            # AllGather
+            items, _, _ = _describe(P.PL_COLL_ALL_GATHER, world, P.PL_U8, [S], sres, dres, sm, tune)
+            outs = [np.zeros(world * S, np.uint8) for _ in range(world)]
+            run_items(items, ins, outs, "u8")
+            want = oracle.all_gather(ins)
+            for r in range(world):
+                assert np.array_equal(outs[r], want[r])
+            # AllToAll (per-rank size must split into world chunks)
+            S2 = (S // world) * world
+            if S2:
+                ins2 = [x[:S2].copy() for x in ins]
+                items, _, _ = _describe(P.PL_COLL_ALL_TO_ALL, world, P.PL_U8, [S2], sres, dres, sm, tune)
+                outs = [np.zeros(S2, np.uint8) for _ in range(world)]
+                run_items(items, ins2, outs, "u8")
+                want = oracle.all_to_all(ins2)
+                for r in range(world):
+                    assert np.array_equal(outs[r], want[r])
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 8])
+def test_v_plans(world):
+    for trial in range(6):
+        sm = SMS[trial % 3]
+        tune = TUNES[trial % len(TUNES)]
+        sres, dres = _res(world, trial % 2 == 0), _res(world, trial % 2 == 0)
+        c = [int(v) for v in RNG.integers(0, 300, size=world)]
+        c[0] = 0 if world > 1 else c[0]
+        ins = [RNG.integers(0, 256, size=c[s], dtype=np.uint8) for s in range(world)]
+        items, _, _ = _describe(P.PL_COLL_ALL_GATHER_V, world, P.PL_U8, c, sres, dres, sm, tune)
+        outs = [np.zeros(sum(c), np.uint8) for _ in range(world)]
+        run_items(items, ins, outs, "u8")
+        want = oracle.all_gather_v(ins, c)
+        for r in range(world):
+            assert np.array_equal(outs[r], want[r])
+        C = RNG.integers(0, 200, size=(world, world))
+        C[0, 0] = 0
+        ins = [RNG.integers(0, 256, size=int(C[s].sum()), dtype=np.uint8) for s in range(world)]
+        items, _, _ = _describe(P.PL_COLL_ALL_TO_ALL_V, world, P.PL_U8, C.reshape(-1).tolist(), sres, dres, sm, tune)
+        outs = [np.zeros(int(C[:, d].sum()), np.uint8) for d in range(world)]
+        run_items(items, ins, outs, "u8")
+        want = oracle.all_to_all_v(ins, C)
+        for r in range(world):
+            assert np.array_equal(outs[r], want[r])
+
+
+def test_grid_scales_with_work():
+    _, g_small, _ = _describe(P.PL_COLL_ALL_GATHER, 8, P.PL_U8, [1024])
+    _, g_big, _ = _describe(P.PL_COLL_ALL_GATHER, 8, P.PL_U8, [256 << 20])
+    assert 1 <= g_small < g_big <= 2 * 152
+
+
+def test_full_size_plans_are_balanced():
+    """The workload sizes: CTAs get equal byte shares (within one 16-byte granule)."""
+    for coll, world, dtype, sizes in [
+        (P.PL_COLL_ALL_REDUCE, 8, P.PL_BF16, [64 << 20]),
+        (P.PL_COLL_REDUCE_SCATTER, 8, P.PL_F32, [256 << 20]),
+        (P.PL_COLL_ALL_GATHER, 8, P.PL_U8, [256 << 20]),
+        (P.PL_COLL_ALL_TO_ALL, 8, P.PL_U8, [256 << 20]),
+    ]:
+        items, grid, _ = _describe(coll, world, dtype, sizes)
+        per = np.zeros(grid, np.int64)
+        for it in items:
+            per[it["cta"]] += it["len"]
+        assert per.max() - per.min() <= 32, (coll, per.min(), per.max())
