@@ -30,6 +30,8 @@ struct DevPlan {
   pl::Plan plan;
   const void* fn = nullptr;
   int threads = 0;
+  int smem = 0;              // dynamic shared memory (bulk path ring)
+  uint32_t ring_chunk = 0;   // bulk path: bytes per source tile in a slot
   void* d_mem = nullptr;     // items, then cta_begin
   void* h_mem = nullptr;     // pinned host copy (kept: a captured upload replays from it)
   size_t bytes = 0;
@@ -83,7 +85,17 @@ bool capturing(cudaStream_t s) {
   return st != cudaStreamCaptureStatusNone;
 }
 
+// Largest dynamic shared memory a CTA may use on sm_100-class GPUs (227 KiB),
+// less room for the kernels' static shared memory.
+constexpr int kMaxDynSmem = 227 * 1024 - 1024;
+
 const void* pick_kernel(const pl::Plan& p) {
+  if (p.tune.path == pl::kPathBulk) {
+    if (p.nsrc <= 1) return pl::kernel_bulk_copy();
+    if (p.dtype == pl::kF32) return pl::kernel_bulk_reduce_f32(p.nsrc);
+    if (p.dtype == pl::kBF16) return pl::kernel_bulk_reduce_bf16(p.nsrc);
+    return nullptr;
+  }
   if (p.nsrc <= 1) {
     int u = p.tune.unroll;
     u = u >= 8 ? 8 : u >= 4 ? 4 : u >= 2 ? 2 : 1;
@@ -175,10 +187,25 @@ purlin_status get_plan(purlin_ctx* h, int coll, int world, int dtype, const uint
   d->fn = pick_kernel(d->plan);
   if (!d->fn) return PL_ERR_UNSUPPORTED;
   d->threads = d->plan.tune.threads;
+  if (d->plan.tune.path == pl::kPathBulk) {
+    // ring of `stages` slots; a reduce slot holds nsrc input tiles and one output tile
+    const int tiles = d->plan.nsrc > 1 ? d->plan.nsrc + 1 : 1;
+    const int stages = d->plan.tune.stages;
+    int64_t ch = d->plan.tune.chunk_bytes;
+    const int64_t fit = kMaxDynSmem / (int64_t)(stages * tiles);
+    if (ch > fit) ch = fit;
+    if (ch > (1 << 20) / tiles) ch = (1 << 20) / tiles;  // mbarrier transaction count stays below 2^20
+    ch &= ~(int64_t)15;
+    if (ch < 16) return PL_ERR_INVALID_ARG;
+    d->ring_chunk = (uint32_t)ch;
+    d->smem = (int)(stages * tiles * ch);
+    cudaError_t e = cudaFuncSetAttribute(d->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, d->smem);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   if (d->plan.strided) {
     // CTAs of this plan wait on each other: all of them must be resident.
     int occ = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, d->fn, d->threads, 0);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, d->fn, d->threads, d->smem);
     if (e != cudaSuccess) return cuda_fail(e);
     if (occ < 1) return PL_ERR_LAUNCH;
     if (d->plan.grid > occ * h->sm_count) {
@@ -245,13 +272,15 @@ purlin_status run(purlin_ctx* h, int coll, int world, int dtype, const uint64_t*
   a.drop_notify = h->drop_notify >= 0 ? (uint32_t)(h->drop_notify + 1) : 0u;
   a.nsrc = d->plan.nsrc;
   a.store_hint = d->plan.tune.store_hint;
+  a.stages = d->plan.tune.stages;
+  a.chunk_bytes = d->ring_chunk;
   h->drop_notify = -1;
 
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3((unsigned)d->plan.grid);
   cfg.blockDim = dim3((unsigned)d->threads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = (size_t)d->smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   if (d->plan.strided) {

@@ -28,6 +28,8 @@ struct KArgs {
   uint32_t drop_notify;       // 1 + item whose notify is skipped, or 0
   int nsrc;                   // sources of each reduce item
   int store_hint;             // 1 write-back, 2 streaming
+  int stages;                 // bulk path: slots in the shared-memory ring
+  uint32_t chunk_bytes;       // bulk path: bytes per source tile in a slot
 };
 
 // Kernel entry points (device function addresses), by variant.  nullptr when
@@ -35,5 +37,9 @@ struct KArgs {
 const void* kernel_copy(int unroll);
 const void* kernel_reduce_f32(int nsrc, int unroll);
 const void* kernel_reduce_bf16(int nsrc, int unroll);
+// TMA bulk pipeline variants (dynamic shared memory).
+const void* kernel_bulk_copy();
+const void* kernel_bulk_reduce_f32(int nsrc);
+const void* kernel_bulk_reduce_bf16(int nsrc);
 
 }  // namespace pl

@@ -377,9 +377,13 @@ __global__ void __launch_bounds__(512, 2) snac_kernel(const __grid_constant__ KA
   }
   if (threadIdx.x == 0) s_epoch = a.strided ? ld_volatile(&a.ctl[kCtlEpoch]) + 1u : 0u;
 
+  // Thread 0 keeps the next item in registers so its load overlaps the current one.
+  Item next;
+  if (threadIdx.x == 0 && begin < end) next = a.items[begin];
   for (uint32_t i = begin; i < end; i += step) {
     if (threadIdx.x == 0) {
-      const Item it = a.items[i];
+      const Item it = next;
+      if (i + step < end) next = a.items[i + step];
       int ns = 0, nd = 0;
       for (uint32_t m = it.src_mask; m; m &= m - 1) {
         const int b = __ffs(m) - 1;

@@ -41,6 +41,11 @@ struct Piece {
 };
 
 constexpr uint64_t kMaxItemBytes = 1ull << 30;
+// CTA shares are cut at multiples of 512 bytes from a piece's start, so that a
+// warp's 32 x 16-byte vectors cover whole 128-byte lines and 32-byte sectors
+// (a cut at 16 bytes leaves every warp straddling one extra line and two
+// partial sectors, which cost DRAM fills).
+constexpr uint64_t kSplitGranule = 512;
 
 inline uint32_t all_ranks(int world) { return (world >= 32) ? 0xFFFFFFFFu : ((1u << world) - 1u); }
 inline uint64_t ceil_div(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
@@ -353,7 +358,7 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
     uint64_t W = 0;
     for (const Piece& q : pieces) W += q.len;
     uint64_t G = std::max<uint64_t>(1, std::min<uint64_t>(gcap, ceil_div(W, (uint64_t)p.tune.min_cta_bytes)));
-    G = std::min<uint64_t>(G, std::max<uint64_t>(1, W / 16));
+    G = std::min<uint64_t>(G, std::max<uint64_t>(1, W / kSplitGranule));
     p.grid = (int)G;
     std::vector<uint64_t> start(pieces.size() + 1, 0);
     for (size_t i = 0; i < pieces.size(); ++i) start[i + 1] = start[i] + pieces[i].len;
@@ -365,7 +370,7 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
         return;
       }
       pi = (size_t)(std::upper_bound(start.begin(), start.end(), b) - start.begin()) - 1;
-      off = (b - start[pi]) & ~(uint64_t)15;
+      off = (b - start[pi]) & ~(kSplitGranule - 1);
     };
     size_t cp = 0;
     uint64_t co = 0;

@@ -12,3 +12,9 @@ if HERE not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (runs the CUDA library)")
     config.addinivalue_line("markers", "slow: long CPU test")
+
+
+def pytest_sessionstart(session):
+    # (Re)build the C-ABI library when its sources changed; a no-op otherwise.
+    from collective_datapath_reduce_gb300 import _build
+    _build.build()

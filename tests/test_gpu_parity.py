@@ -219,8 +219,10 @@ def test_copies_at_any_byte_alignment():
             want = oracle.all_gather(ins)
             for r in range(world):
                 assert np.array_equal(outs[r], want[r]), (smis, dmis, S)
-            outs = run_copy("a2a", world, ins, S, [S] * world, smis, dmis)
-            want = oracle.all_to_all(ins)
+            S2 = S - S % world
+            ins2 = [x[:S2].copy() for x in ins]
+            outs = run_copy("a2a", world, ins2, S2, [S2] * world, smis, dmis)
+            want = oracle.all_to_all(ins2)
             for r in range(world):
                 assert np.array_equal(outs[r], want[r]), (smis, dmis, S)
 
@@ -428,6 +430,118 @@ def test_consume_wait_runs_out_and_recovers():
     assert h.status() == P.PL_ERR_TIMEOUT
     assert h.status() == 0                                # reading clears it
     dst.fill(0)
+    P.check(P.purlin_all_reduce(h.h, src.ptrs(), dst.ptrs(), n * 4, P.PL_F32, 0, stream()))
+    sync()
+    assert h.status() == 0
+    assert h.close() == P.PL_OK
+    want = oracle.all_reduce(ins, "f32")
+    for r in range(world):
+        assert np.array_equal(bits(dst.read(r, np.float32)), bits(want[r]))
+
+
+# ------------------------------------------------------ TMA bulk pipeline
+
+BULK = {"path": P.PATH_BULK}
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("world", [2, 3, 8, 11])
+@pytest.mark.parametrize("stages,chunk", [(2, 4096), (3, 16384), (4, 65536)])
+def test_bulk_all_reduce(dtype, world, stages, chunk):
+    tune = dict(BULK, stages=stages, chunk_bytes=chunk)
+    for n in (8, 1000, 65536 + 24, (1 << 20) + 8):
+        for layout in (P.PL_LAYOUT_ONE_SHOT, P.PL_LAYOUT_TWO_SHOT):
+            ins, outs = run_all_reduce(world, dtype, n, layout, tune=tune)
+            want = oracle.all_reduce(ins, dtype)
+            for r in range(world):
+                assert np.array_equal(bits(outs[r]), bits(want[r])), (n, layout, r)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_bulk_unaligned_and_in_place(dtype):
+    E = ESZ[dtype]
+    tune = dict(BULK, stages=3, chunk_bytes=8192)
+    ins, outs = run_all_reduce(4, dtype, 50001, P.PL_LAYOUT_ONE_SHOT, misalign=[E, 0, 2 * E, 0], tune=tune)
+    want = oracle.all_reduce(ins, dtype)
+    for r in range(4):
+        assert np.array_equal(bits(outs[r]), bits(want[r]))
+    world, n = 8, 300000
+    ins = [draw(dtype, n) for _ in range(world)]
+    buf = RankBuffers([n * E] * world)
+    buf.upload(ins)
+    h = Handle(world)
+    P.check(P.purlin_tune_override(h.h, tune))
+    P.check(P.purlin_all_reduce(h.h, buf.ptrs(), buf.ptrs(), n * E, DT[dtype], 0, stream()))
+    sync()
+    assert h.close() == P.PL_OK
+    want = oracle.all_reduce(ins, dtype)
+    for r in range(world):
+        assert np.array_equal(bits(buf.read(r, NP[dtype])), bits(want[r]))
+
+
+@pytest.mark.parametrize("stages,chunk", [(2, 4096), (4, 32768)])
+def test_bulk_copies_and_reduce_scatter(stages, chunk):
+    tune = dict(BULK, stages=stages, chunk_bytes=chunk)
+    world = 8
+    for S in (16, 4096, 65536 + 48, (1 << 20) + 16 * 8):
+        ins = [RNG.integers(0, 256, size=S, dtype=np.uint8) for _ in range(world)]
+        outs = run_copy("ag", world, ins, S, [world * S] * world, tune=tune)
+        want = oracle.all_gather(ins)
+        for r in range(world):
+            assert np.array_equal(outs[r], want[r])
+        outs = run_copy("a2a", world, ins, S, [S] * world, tune=tune)
+        want = oracle.all_to_all(ins)
+        for r in range(world):
+            assert np.array_equal(outs[r], want[r])
+    # unaligned byte buffers fall back to the register path inside the bulk kernel
+    ins = [RNG.integers(0, 256, size=1003, dtype=np.uint8) for _ in range(4)]
+    outs = run_copy("ag", 4, ins, 1003, [4 * 1003] * 4, [1, 2, 3, 4], [5, 0, 7, 0], tune=tune)
+    want = oracle.all_gather(ins)
+    for r in range(4):
+        assert np.array_equal(outs[r], want[r])
+    C, c = inputs.w5_counts(world, max_count=20000, seed=4)
+    a2av_in, agv_in = inputs.w5_payloads(C, c, seed=4)
+    outs = run_copy("agv", world, agv_in, [int(v) * 2 for v in c], [int(c.sum()) * 2] * world, tune=tune)
+    want = oracle.all_gather_v(agv_in, [int(v) for v in c])
+    for r in range(world):
+        assert np.array_equal(outs[r].view(np.uint16), want[r])
+    outs = run_copy("a2av", world, a2av_in, [int(v) * 2 for v in C.reshape(-1)],
+                    [int(C[:, d].sum()) * 2 for d in range(world)], tune=tune)
+    want = oracle.all_to_all_v(a2av_in, C)
+    for r in range(world):
+        assert np.array_equal(outs[r].view(np.uint16), want[r])
+    for dtype in ("f32", "bf16"):
+        E = ESZ[dtype]
+        chunk_e = 70001
+        n = chunk_e * world
+        ins = [draw(dtype, n) for _ in range(world)]
+        src = RankBuffers([n * E] * world)
+        dst = RankBuffers([chunk_e * E] * world)
+        src.upload(ins)
+        h = Handle(world)
+        P.check(P.purlin_tune_override(h.h, tune))
+        P.check(P.purlin_reduce_scatter(h.h, src.ptrs(), dst.ptrs(), n * E, DT[dtype], 0, stream()))
+        sync()
+        assert h.close() == P.PL_OK
+        want = oracle.reduce_scatter(ins, dtype)
+        for r in range(world):
+            assert np.array_equal(bits(dst.read(r, NP[dtype])), bits(want[r]))
+        assert dst.guards_intact()
+
+
+def test_bulk_consume_wait_runs_out_and_recovers():
+    world, n = 4, 1 << 16
+    ins = [draw("f32", n) for _ in range(world)]
+    src = RankBuffers([n * 4] * world)
+    dst = RankBuffers([n * 4] * world)
+    src.upload(ins)
+    h = Handle(world)
+    P.check(P.purlin_tune_override(h.h, dict(BULK, layout=P.PL_LAYOUT_TWO_SHOT, chunk_bytes=4096, stages=2)))
+    P.check(P.purlin_set_wait_timeout_ns(h.h, 20_000_000))
+    P.check(P.purlin_debug_drop_notify(h.h, 1))
+    P.check(P.purlin_all_reduce(h.h, src.ptrs(), dst.ptrs(), n * 4, P.PL_F32, 0, stream()))
+    sync()
+    assert h.status() == P.PL_ERR_TIMEOUT
     P.check(P.purlin_all_reduce(h.h, src.ptrs(), dst.ptrs(), n * 4, P.PL_F32, 0, stream()))
     sync()
     assert h.status() == 0
