@@ -318,6 +318,14 @@ purlin_status check_ptrs(const void* const* p, int n) {
   return PL_OK;
 }
 
+// Pointers may be NULL only where the rank's buffer holds zero bytes.
+purlin_status check_ptrs_sized(const void* const* p, int n, const std::vector<uint64_t>& bytes) {
+  if (!p) return PL_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i)
+    if (!p[i] && bytes[(size_t)i]) return PL_ERR_INVALID_ARG;
+  return PL_OK;
+}
+
 purlin_status check_reduce_args(purlin_dtype dtype, purlin_mode mode) {
   if (mode != PL_DETERMINISTIC) return PL_ERR_UNSUPPORTED;
   if (dtype != PL_F32 && dtype != PL_BF16) return PL_ERR_UNSUPPORTED;
@@ -462,7 +470,6 @@ purlin_status purlin_reduce_scatter_v(purlin_handle h, const void* const* src, v
   if ((st = check_handle(h)) || (st = check_reduce_args(dtype, mode))) return st;
   const int N = h->world;
   if (!bytes) return PL_ERR_INVALID_ARG;
-  if ((st = check_ptrs(src, N)) || (st = check_ptrs((const void* const*)dst, N))) return st;
   const size_t E = (size_t)pl::elem_size(dtype);
   std::vector<uint64_t> sz((size_t)N), bi((size_t)N);
   uint64_t total = 0;
@@ -471,10 +478,11 @@ purlin_status purlin_reduce_scatter_v(purlin_handle h, const void* const* src, v
     sz[r] = bytes[r];
     total += bytes[r];
   }
+  std::fill(bi.begin(), bi.end(), total);
+  if ((st = check_ptrs_sized(src, N, bi)) || (st = check_ptrs_sized((const void* const*)dst, N, sz))) return st;
   if ((st = check_elem_aligned(src, N, E)) || (st = check_elem_aligned((const void* const*)dst, N, E)))
     return st;
   if (total == 0) return PL_OK;
-  std::fill(bi.begin(), bi.end(), total);
   if ((st = check_overlap(ranges(src, N, bi), ranges((const void* const*)dst, N, sz), false))) return st;
   return run(h, pl::kReduceScatterV, N, dtype, sz.data(), sz.size(), src, N, dst, N, (cudaStream_t)stream);
 }
@@ -512,15 +520,15 @@ purlin_status purlin_all_gather_v(purlin_handle h, const void* const* src, void*
   if ((st = check_handle(h))) return st;
   const int N = h->world;
   if (!bytes) return PL_ERR_INVALID_ARG;
-  if ((st = check_ptrs(src, N)) || (st = check_ptrs((const void* const*)dst, N))) return st;
   std::vector<uint64_t> sz((size_t)N), bo((size_t)N);
   uint64_t total = 0;
   for (int r = 0; r < N; ++r) {
     sz[r] = bytes[r];
     total += bytes[r];
   }
-  if (total == 0) return PL_OK;
   std::fill(bo.begin(), bo.end(), total);
+  if ((st = check_ptrs_sized(src, N, sz)) || (st = check_ptrs_sized((const void* const*)dst, N, bo))) return st;
+  if (total == 0) return PL_OK;
   if ((st = check_overlap(ranges(src, N, sz), ranges((const void* const*)dst, N, bo), false))) return st;
   return run(h, pl::kAllGatherV, N, pl::kU8, sz.data(), sz.size(), src, N, dst, N, (cudaStream_t)stream);
 }
@@ -531,7 +539,6 @@ purlin_status purlin_all_to_all_v(purlin_handle h, const void* const* src, void*
   if ((st = check_handle(h))) return st;
   const int N = h->world;
   if (!bytes) return PL_ERR_INVALID_ARG;
-  if ((st = check_ptrs(src, N)) || (st = check_ptrs((const void* const*)dst, N))) return st;
   std::vector<uint64_t> sz((size_t)N * N), bi((size_t)N, 0), bo((size_t)N, 0);
   uint64_t total = 0;
   for (int s = 0; s < N; ++s)
@@ -542,6 +549,7 @@ purlin_status purlin_all_to_all_v(purlin_handle h, const void* const* src, void*
       bo[d] += c;
       total += c;
     }
+  if ((st = check_ptrs_sized(src, N, bi)) || (st = check_ptrs_sized((const void* const*)dst, N, bo))) return st;
   if (total == 0) return PL_OK;
   if ((st = check_overlap(ranges(src, N, bi), ranges((const void* const*)dst, N, bo), false))) return st;
   return run(h, pl::kAllToAllV, N, pl::kU8, sz.data(), sz.size(), src, N, dst, N, (cudaStream_t)stream);

@@ -95,25 +95,87 @@ size_t n_sizes(int coll, int world) {
   }
 }
 
-// Initial tuning table.  Entries are replaced by the measured sweep; the
-// defaults are what a streaming kernel on 148+ SMs usually wants: two
-// 512-thread CTAs per SM, enough 16-byte loads in flight per thread to cover
-// HBM latency, and no shrinking of the grid until a CTA would get less than
-// 32 KiB of work.
+// Tuning table, from the sweep measured on a GB300 (152 SMs, HBM3e):
+// `bytes_per_rank` is the per-rank size the collective moves (for the V
+// variants, their total divided by the world).  Summary of what won:
+//   AllReduce   register path, 256 threads x 2 CTAs/SM (90% of the measured
+//               copy bandwidth at 8 x 64 MiB bf16); the fewest bytes per CTA
+//               stay at 512 so small calls spread over many CTAs.
+//   ReduceScatter  from 8 MiB per rank the TMA bulk ring (2 slots x 32 KiB
+//               per source) runs above the copy bandwidth: the traffic is
+//               8 reads per write.  Below that, the register path.
+//   AllGather   from 4 MiB per rank the bulk ring (4 slots x 4 KiB): one load,
+//               eight bulk stores per chunk.  Below, register copies.
+//   AllToAll    from 32 MiB per rank the bulk ring (3 x 32 KiB); below,
+//               register copies with streaming stores.
 Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
   (void)dtype;
-  (void)bytes_per_rank;
+  const uint64_t S = bytes_per_rank;
+  constexpr uint64_t KiB = 1024, MiB = 1024 * 1024;
   Tune t;
-  const bool red = is_reduce_coll(coll);
   t.layout = kOneShot;
   t.path = kPathRegister;
-  t.threads = 512;
+  t.threads = 256;
   t.ctas_per_sm = 2;
-  t.unroll = red ? (world <= 4 ? 2 : 1) : 4;
-  t.chunk_bytes = 64 * 1024;
-  t.stages = 4;
+  t.unroll = 4;
+  t.chunk_bytes = 32 * 1024;
+  t.stages = 3;
   t.store_hint = 1;
-  t.min_cta_bytes = 32 * 1024;
+  t.min_cta_bytes = 512;
+  switch (coll) {
+    case kAllReduce:
+    case kAtomReduce:
+      t.unroll = world <= 4 ? 2 : 1;
+      t.chunk_bytes = 64 * 1024;  // two-shot tile
+      if (S <= 4 * MiB) t.threads = 512;
+      break;
+    case kReduceScatter:
+    case kReduceScatterV:
+      t.unroll = world <= 4 ? 2 : 1;
+      if (S >= 8 * MiB) {
+        t.path = kPathBulk;
+        t.ctas_per_sm = 1;
+        t.stages = 2;
+        t.chunk_bytes = 32 * 1024;
+      } else {
+        t.ctas_per_sm = 3;
+        t.store_hint = 2;
+      }
+      break;
+    case kAllGather:
+    case kAllGatherV:
+    case kAtomCopy:
+      if (S >= 4 * MiB) {
+        t.path = kPathBulk;
+        t.ctas_per_sm = 1;
+        t.stages = 4;
+        t.chunk_bytes = 4 * 1024;
+      } else if (S >= 256 * KiB) {
+        t.threads = 512;
+        t.min_cta_bytes = 2 * 1024;
+      }
+      break;
+    case kAllToAll:
+    case kAllToAllV:
+      if (S >= 32 * MiB) {
+        t.path = kPathBulk;
+        t.ctas_per_sm = 1;
+        t.stages = 3;
+        t.chunk_bytes = 32 * 1024;
+      } else {
+        t.unroll = 2;
+        t.store_hint = 2;
+        if (S >= 1 * MiB) {
+          t.threads = 512;
+          t.min_cta_bytes = 32 * 1024;
+        } else if (S >= 128 * KiB) {
+          t.min_cta_bytes = 8 * 1024;
+        } else {
+          t.min_cta_bytes = 2 * 1024;
+        }
+      }
+      break;
+  }
   return t;
 }
 
@@ -166,7 +228,13 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
   p.dtype = dtype;
   p.elem = red ? elem_size(dtype) : 1;
   const uint64_t E = (uint64_t)p.elem;
-  p.tune = tune_merge(tune_table(coll, world, dtype, sizes[0]), tune_in);
+  uint64_t per_rank = sizes[0];
+  if (coll == kAllGatherV || coll == kAllToAllV || coll == kReduceScatterV) {
+    uint64_t total = 0;
+    for (size_t i = 0; i < nsizes; ++i) total += sizes[i];
+    per_rank = total / (uint64_t)world;
+  }
+  p.tune = tune_merge(tune_table(coll, world, dtype, per_rank), tune_in);
   if (int st = validate_tune(p.tune)) return st;
   if (max_ctas_per_sm > 0) p.tune.ctas_per_sm = std::min(p.tune.ctas_per_sm, max_ctas_per_sm);
 

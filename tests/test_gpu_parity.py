@@ -549,3 +549,35 @@ def test_bulk_consume_wait_runs_out_and_recovers():
     want = oracle.all_reduce(ins, "f32")
     for r in range(world):
         assert np.array_equal(bits(dst.read(r, np.float32)), bits(want[r]))
+
+
+def test_v_variants_accept_null_for_empty_ranks():
+    world = 3
+    c = [5, 0, 7]
+    ins = [RNG.integers(0, 256, size=v, dtype=np.uint8) for v in c]
+    src = RankBuffers([max(v, 1) for v in c])
+    src.upload([x if x.size else np.zeros(1, np.uint8) for x in ins])
+    dst = RankBuffers([sum(c)] * world)
+    sp = src.ptrs()
+    sp[1] = 0                                   # a zero-byte rank may pass NULL
+    h = Handle(world)
+    P.check(P.purlin_all_gather_v(h.h, sp, dst.ptrs(), c, stream()))
+    sync()
+    want = oracle.all_gather_v(ins, c)
+    for r in range(world):
+        assert np.array_equal(dst.read(r), want[r])
+    C = np.array([[2, 0, 1], [0, 0, 0], [3, 0, 4]])
+    ins = [RNG.integers(0, 256, size=int(C[s].sum()), dtype=np.uint8) for s in range(world)]
+    src = RankBuffers([max(int(C[s].sum()), 1) for s in range(world)])
+    src.upload([x if x.size else np.zeros(1, np.uint8) for x in ins])
+    dst = RankBuffers([max(int(C[:, d].sum()), 1) for d in range(world)])
+    sp, dp = src.ptrs(), dst.ptrs()
+    sp[1] = 0
+    dp[1] = 0
+    P.check(P.purlin_all_to_all_v(h.h, sp, dp, C.reshape(-1).tolist(), stream()))
+    sync()
+    want = oracle.all_to_all_v(ins, C)
+    for d in (0, 2):
+        assert np.array_equal(dst.read(d)[:want[d].size], want[d])
+    assert P.purlin_all_gather_v(h.h, [0, 0, 0], dst.ptrs(), [1, 0, 0], stream()) == P.PL_ERR_INVALID_ARG
+    assert h.close() == P.PL_OK
