@@ -8,9 +8,13 @@ is HBM GB/s counted as algorithmic bytes (every input byte read once, every
 output byte written once: 2 * 8 * 64 MiB = 1 GiB per step) over device time.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl own|reference]
+                  [--workload NAME]
 
 Prints one JSON line (rank 0).  With --impl reference the CPU oracle is timed
 on the host cores on a bounded sample of the same workload instead.
+--workload picks another of the five workloads' largest cases (ReduceScatter,
+AllGather, AllToAll, AllToAllV, AllGatherV) for the same measurement; the
+default is the AllReduce above.
 """
 
 from __future__ import annotations
@@ -40,6 +44,59 @@ WORKLOAD = "AllReduce sum, 8 emulated ranks on one GPU, bf16 in/out, fp32 ascend
            "32 Mi elements (64 MiB) per rank, N(0,1), seed 1"
 
 
+class Workload:
+    """One collective at one workload size: host inputs, output sizes, the call, its bytes."""
+
+    def __init__(self, name, desc, dtype, make_inputs, out_bytes, call, algo_bytes, coll, tune_bytes):
+        self.name, self.desc, self.dtype = name, desc, dtype
+        self.make_inputs, self.out_bytes, self.call = make_inputs, out_bytes, call
+        self.algo_bytes, self.coll, self.tune_bytes = algo_bytes, coll, tune_bytes
+
+
+def workloads(P, inputs):
+    """The five workloads' largest single-GPU cases (the first is the headline)."""
+    MI = 1 << 20
+    C5, c5 = inputs.w5_counts(WORLD)
+    w = [
+        Workload("allreduce_bf16_8x64MiB", WORKLOAD, "bf16",
+                 lambda: list(inputs.w2_allreduce_bf16(WORLD, N_ELEMS, seed=1)),
+                 [S] * WORLD, lambda h, s, d, st: P.purlin_all_reduce(h, s, d, S, P.PL_BF16, 0, st),
+                 ALGO_BYTES, P.PL_COLL_ALL_REDUCE, S),
+        Workload("reduce_scatter_f32_8x256MiB",
+                 "ReduceScatter sum, 8 ranks, fp32, 64 Mi elements (256 MiB) per rank, U(-1,1), seed 2", "f32",
+                 lambda: list(inputs.w3_reduce_scatter(WORLD, 64 * MI, seed=2, dtype="f32")),
+                 [32 * MI] * WORLD, lambda h, s, d, st: P.purlin_reduce_scatter(h, s, d, 256 * MI, P.PL_F32, 0, st),
+                 WORLD * 256 * MI + 256 * MI, P.PL_COLL_REDUCE_SCATTER, 256 * MI),
+        Workload("reduce_scatter_bf16_8x128MiB",
+                 "ReduceScatter sum, 8 ranks, bf16, 64 Mi elements (128 MiB) per rank, U(-1,1), seed 2", "bf16",
+                 lambda: list(inputs.w3_reduce_scatter(WORLD, 64 * MI, seed=2, dtype="bf16")),
+                 [16 * MI] * WORLD, lambda h, s, d, st: P.purlin_reduce_scatter(h, s, d, 128 * MI, P.PL_BF16, 0, st),
+                 WORLD * 128 * MI + 128 * MI, P.PL_COLL_REDUCE_SCATTER, 128 * MI),
+        Workload("all_gather_u8_8x256MiB", "AllGather, 8 ranks, uint8 payload, 256 MiB per rank, seed 3", "u8",
+                 lambda: list(inputs.w4_bytes(WORLD, 256 * MI)),
+                 [WORLD * 256 * MI] * WORLD, lambda h, s, d, st: P.purlin_all_gather(h, s, d, 256 * MI, st),
+                 WORLD * 256 * MI * (1 + WORLD), P.PL_COLL_ALL_GATHER, 256 * MI),
+        Workload("all_to_all_u8_8x256MiB", "AllToAll, 8 ranks, uint8 payload, 256 MiB per rank, seed 3", "u8",
+                 lambda: list(inputs.w4_bytes(WORLD, 256 * MI)),
+                 [256 * MI] * WORLD, lambda h, s, d, st: P.purlin_all_to_all(h, s, d, 256 * MI, st),
+                 2 * WORLD * 256 * MI, P.PL_COLL_ALL_TO_ALL, 256 * MI),
+        Workload("all_to_all_v_bf16_w5",
+                 "AllToAllV, 8 ranks, bf16 N(0,1), counts uniform in [0, 4 Mi] elements with forced zeros and "
+                 "counts not multiple of 8, seed 4", "bf16",
+                 lambda: inputs.w5_payloads(C5, c5)[0],
+                 [int(C5[:, d].sum()) * 2 for d in range(WORLD)],
+                 lambda h, s, d, st: P.purlin_all_to_all_v(h, s, d, [int(v) * 2 for v in C5.reshape(-1)], st),
+                 2 * int(C5.sum()) * 2, P.PL_COLL_ALL_TO_ALL_V, int(C5.sum()) * 2 // WORLD),
+        Workload("all_gather_v_bf16_w5",
+                 "AllGatherV, 8 ranks, bf16 N(0,1), counts uniform in [0, 4 Mi] elements, seed 4", "bf16",
+                 lambda: inputs.w5_payloads(C5, c5)[1],
+                 [int(c5.sum()) * 2] * WORLD,
+                 lambda h, s, d, st: P.purlin_all_gather_v(h, s, d, [int(v) * 2 for v in c5], st),
+                 int(c5.sum()) * 2 * (1 + WORLD), P.PL_COLL_ALL_GATHER_V, int(c5.sum()) * 2 // WORLD),
+    ]
+    return {x.name: x for x in w}
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -48,6 +105,8 @@ def parse():
     ap.add_argument("--impl", choices=["own", "reference"], default="own")
     ap.add_argument("--no-extras", action="store_true", help="skip the per-collective side table")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--workload", default="allreduce_bf16_8x64MiB",
+                    help="which collective to time (default: the AllReduce headline)")
     return ap.parse_args()
 
 
@@ -163,10 +222,10 @@ def source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes per launch of the AllReduce kernel from the committed ncu summary,
+def recorded_traffic(name):
+    """DRAM bytes per launch of the workload's kernel from the committed ncu summary,
     or None when the kernel sources changed since the counters were taken."""
-    p = os.path.join(ROOT, "profiles", "allreduce_bf16_8x64MiB.traffic.json")
+    p = os.path.join(ROOT, "profiles", f"{name}.traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
@@ -190,15 +249,17 @@ def run_own(args, dist):
     torch.cuda.set_device(dev)
     dist.init("nccl")
     stream = torch.cuda.Stream(device=dev)
+    wl = workloads(P, inputs)[args.workload]
+    headline = args.workload == "allreduce_bf16_8x64MiB"
 
-    x = inputs.w2_allreduce_bf16(WORLD, N_ELEMS, seed=1)          # host, (8, 32 Mi) bf16 bits
-    host_in = [torch.from_numpy(x[r].view(np.int16)).pin_memory() for r in range(WORLD)]
-    src = [torch.empty(N_ELEMS, dtype=torch.int16, device=dev) for _ in range(WORLD)]
-    dst = [torch.empty(N_ELEMS, dtype=torch.int16, device=dev) for _ in range(WORLD)]
-    host_out = [torch.empty(N_ELEMS, dtype=torch.int16).pin_memory() for _ in range(WORLD)]
+    x = wl.make_inputs()                                      # host arrays, one per rank
+    host_in = [torch.from_numpy(np.ascontiguousarray(a).view(np.uint8)).pin_memory() for a in x]
+    src = [torch.empty(max(t.numel(), 1), dtype=torch.uint8, device=dev) for t in host_in]
+    dst = [torch.empty(max(b, 1), dtype=torch.uint8, device=dev) for b in wl.out_bytes]
     with torch.cuda.stream(stream):
         for r in range(WORLD):
-            src[r].copy_(host_in[r], non_blocking=True)
+            if host_in[r].numel():
+                src[r][:host_in[r].numel()].copy_(host_in[r], non_blocking=True)
     stream.synchronize()
 
     st, h = P.purlin_initialize(WORLD, None, 0, stream)
@@ -207,14 +268,15 @@ def run_own(args, dist):
     dptr = [t.data_ptr() for t in dst]
 
     def step():
-        st = P.purlin_all_reduce(h, sptr, dptr, S, P.PL_BF16, P.PL_DETERMINISTIC, stream)
+        st = wl.call(h, sptr, dptr, stream)
         if st != P.PL_OK:
-            raise P.PurlinError(st, "purlin_all_reduce")
+            raise P.PurlinError(st, wl.name)
 
     for _ in range(args.warmup):
         step()
     stream.synchronize()
-    _, tune = P.purlin_tune_get(h, P.PL_COLL_ALL_REDUCE, P.PL_BF16, S)
+    _, tune = P.purlin_tune_get(h, wl.coll, {"bf16": P.PL_BF16, "f32": P.PL_F32, "u8": P.PL_U8}[wl.dtype],
+                                wl.tune_bytes)
 
     clocks = ClockSampler(dist.local)
     clocks.start()
@@ -245,10 +307,13 @@ def run_own(args, dist):
 
     total_ms = dist.max(total_ms, dev)
     ms_per_step = total_ms / K
-    value = dist.world * ALGO_BYTES * K / (total_ms / 1e3) / 1e9
+    value = dist.world * wl.algo_bytes * K / (total_ms / 1e3) / 1e9
 
-    # end to end: host buffers in, result back to host, every step
-    Ke = max(3, min(K, 20))
+    # end to end: host buffers in, results back to host, every step
+    host_out = [torch.empty(b, dtype=torch.uint8).pin_memory() for b in wl.out_bytes]
+    in_bytes = sum(t.numel() for t in host_in)
+    out_bytes = sum(wl.out_bytes)
+    Ke = max(3, min(K, 20, int((4 << 30) // max(in_bytes + out_bytes, 1))))
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     dist.barrier()
@@ -257,42 +322,46 @@ def run_own(args, dist):
     with torch.cuda.stream(stream):
         for _ in range(Ke):
             for r in range(WORLD):
-                src[r].copy_(host_in[r], non_blocking=True)
+                if host_in[r].numel():
+                    src[r][:host_in[r].numel()].copy_(host_in[r], non_blocking=True)
             step()
             for r in range(WORLD):
-                host_out[r].copy_(dst[r], non_blocking=True)
+                if wl.out_bytes[r]:
+                    host_out[r].copy_(dst[r][:wl.out_bytes[r]], non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     dist.barrier()
     e2e_ms = dist.max(e0.elapsed_time(e1), dev) / Ke
-    e2e = {"value": round(dist.world * ALGO_BYTES / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
-           "h2d_bytes_per_step": WORLD * S, "d2h_bytes_per_step": WORLD * S, "ms_per_step": round(e2e_ms, 4)}
+    e2e = {"value": round(dist.world * wl.algo_bytes / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes, "ms_per_step": round(e2e_ms, 4),
+           "steps": Ke}
 
     peak, peak_kind = measured_peaks()
-    achieved = ALGO_BYTES / (kernel_ms / 1e3) / 1e9
+    achieved = wl.algo_bytes / (kernel_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(),
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(wl.name),
                 "peak_source": f"hbm_gbs of {peak_kind}", "kernel_ms": round(kernel_ms, 5),
-                "algorithmic_bytes_per_launch": ALGO_BYTES}
+                "algorithmic_bytes_per_launch": wl.algo_bytes}
 
     extras = None
-    if not args.no_extras and dist.rank == 0:
+    if headline and not args.no_extras and dist.rank == 0:
         extras = side_table(P, h, stream, dev)
 
     P.check(P.purlin_finalize(h, stream), "purlin_finalize")
 
     cpu = None
-    if dist.rank == 0 and dist.world == 1 and not args.no_cpu:
-        cpu = cpu_baseline(x, budget_s=12.0)
+    if headline and dist.rank == 0 and dist.world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(np.stack(x), budget_s=12.0)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "world": WORLD, "bytes_per_rank": S,
-                   "algorithmic_bytes_per_step": ALGO_BYTES,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.desc, "name": wl.name, "world": WORLD,
+                   "algorithmic_bytes_per_step": wl.algo_bytes,
                    "parallelism": f"replicas{dist.world}" if dist.world > 1 else "single-gpu",
-                   "l2": "inputs 512 MiB and outputs 512 MiB per step exceed the 126 MiB L2; no flush",
+                   "l2": f"inputs {in_bytes >> 20} MiB and outputs {out_bytes >> 20} MiB per step exceed the "
+                         "126 MiB L2; no flush",
                    "tune": tune},
         "roofline": roofline, "e2e": e2e, "gpu_launches": K, "clocks": clk,
         "cpu_baseline": cpu,
