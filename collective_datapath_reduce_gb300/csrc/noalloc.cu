@@ -1,0 +1,280 @@
+// AllReduce that allocates nothing: purlin_all_reduce_noalloc.
+//
+// Some callers may not allocate device memory once they are running: a
+// runtime that fixes its memory at start-up, a plug-in that lives inside
+// another framework's memory pool and must not go around it, or code that
+// cannot afford the device-wide synchronisation cudaMalloc / cudaFree may
+// imply.  They cannot create a handle (its workspace and cached plans are
+// allocated).  This entry point runs the two-shot AllReduce without a handle:
+// its scratch (SNAC flags and control words) is the file-scope array below,
+// and the work items are computed in the kernel instead of being uploaded.
+//
+// The array lives in every GPU that loads the library until the process
+// exits.  Every call on a device shares it and it keeps the last call's
+// contents; flags carry the launch's epoch, so stale values never match and
+// nothing has to be cleared between calls.  Calls that overlap on the GPU
+// (different streams, no ordering) race on the array and must not be made.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "kernels.cuh"
+#include "purlin_gb.h"
+
+namespace pl {
+namespace {
+
+// Control words, then one flag per two-shot tile.
+constexpr int kNaCtlWords = 64;
+constexpr int kNaMaxFlags = 16384;
+constexpr uint64_t kNaTile = 64 * 1024;  // bytes of one owner's range per tile
+constexpr int kNaMaxDevices = 64;
+constexpr int kNaThreads = 512;
+enum : int { kNaEpoch = 0, kNaFailed = 1, kNaDone = 2 };
+
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kNaCtlWords + kNaMaxFlags];
+
+struct NaArgs {
+  const char* in[kMaxWorld];
+  char* out[kMaxWorld];
+  uint32_t* scratch;         // device address of g_noalloc_scratch
+  int* device_status;        // caller's status word, or nullptr
+  unsigned long long timeout_ns;
+  uint64_t q, rem;           // elements per owner, and owners with one more
+  uint32_t elem;             // bytes per element
+  uint32_t world;
+  uint32_t tmax;             // tiles of the largest owner range
+  uint32_t lag;              // rounds between a tile's reduce and its copies
+  uint32_t slots;            // (tmax + lag) rounds of 2 * world slots
+  uint32_t dst_coaligned;    // every output has the same address residue mod 16
+};
+
+// Wait for the flag to hold the launch's epoch.  A failure of this launch is
+// recorded as its epoch in the `failed` word, so an old failure never stops
+// a later call.
+__device__ bool na_wait(const NaArgs& a, const uint32_t* flag, uint32_t epoch) {
+  const unsigned long long t0 = globaltimer();
+  const unsigned long long cap = a.timeout_ns / 16ull + 4096ull;
+  for (unsigned long long spin = 0;; ++spin) {
+    if (ld_acquire(flag) == epoch) return true;
+    if ((spin & 31ull) == 31ull) {
+      if (ld_volatile(a.scratch + kNaFailed) == epoch) return false;
+      if (globaltimer() - t0 > a.timeout_ns || spin > cap) {
+        atomicExch(a.scratch + kNaFailed, epoch);
+        return false;
+      }
+    }
+    __nanosleep(32);
+  }
+}
+
+template <typename T, int NS>
+__global__ void __launch_bounds__(kNaThreads, 2) noalloc_kernel(const __grid_constant__ NaArgs a) {
+  __shared__ const char* s_src[kMaxWorld];
+  __shared__ char* s_dst[kMaxWorld];
+  __shared__ uint64_t s_len;
+  __shared__ int s_ns, s_nd, s_ok, s_kind;  // kind: 0 skip, 1 reduce, 2 copy
+  __shared__ uint32_t s_flag, s_epoch;
+
+  const uint32_t N = a.world;
+  if (threadIdx.x == 0) s_epoch = ld_volatile(a.scratch + kNaEpoch) + 1u;
+  for (uint32_t slot = blockIdx.x; slot < a.slots; slot += gridDim.x) {
+    if (threadIdx.x == 0) {
+      const uint32_t round = slot / (2 * N), k = slot % (2 * N);
+      const bool reduce = k < N;
+      const uint32_t o = reduce ? k : k - N;
+      const int64_t t = reduce ? (int64_t)round : (int64_t)round - (int64_t)a.lag;
+      const uint64_t olen = (a.q + (o < a.rem ? 1 : 0)) * a.elem;
+      const uint64_t ostart = ((uint64_t)o * a.q + (o < a.rem ? o : a.rem)) * a.elem;
+      int kind = 0;
+      if (t >= 0 && (uint64_t)t * kNaTile < olen) kind = reduce ? 1 : 2;
+      if (kind && N == 1 && kind == 2) kind = 0;
+      int ok = 1;
+      if (kind) {
+        const uint64_t off = ostart + (uint64_t)t * kNaTile;
+        const uint64_t rest = olen - (uint64_t)t * kNaTile;
+        s_len = rest < kNaTile ? rest : kNaTile;
+        s_flag = o * a.tmax + (uint32_t)t;
+        if (kind == 1) {
+          for (uint32_t s = 0; s < N; ++s) s_src[s] = a.in[s] + off;
+          s_dst[0] = a.out[o] + off;
+          s_ns = (int)N;
+          s_nd = 1;
+        } else {
+          s_src[0] = a.out[o] + off;
+          int nd = 0;
+          for (uint32_t r = 0; r < N; ++r)
+            if (r != o) s_dst[nd++] = a.out[r] + off;
+          s_ns = 1;
+          s_nd = nd;
+          ok = na_wait(a, a.scratch + kNaCtlWords + s_flag, s_epoch);
+        }
+        if (ok && ld_volatile(a.scratch + kNaFailed) == s_epoch) ok = 0;
+      }
+      s_kind = kind;
+      s_ok = ok;
+    }
+    __syncthreads();
+    if (!s_ok) break;
+    if (s_kind == 1) {
+      if (s_ns == 1)
+        copy_atom<false, 2, false>(s_src[0], s_dst, 1, s_len);
+      else
+        reduce_atom<T, NS, 1, false>(s_src, s_ns, s_dst, 1, s_len);
+    } else if (s_kind == 2) {
+      if (a.dst_coaligned) {
+        copy_atom<true, 2, false>(s_src[0], s_dst, s_nd, s_len);
+      } else {
+        for (int j = 0; j < s_nd; ++j) copy_atom<true, 2, false>(s_src[0], s_dst + j, 1, s_len);
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && s_kind == 1 && N > 1) {
+      __threadfence();
+      st_release(a.scratch + kNaCtlWords + s_flag, s_epoch);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const uint32_t done = atomicAdd(a.scratch + kNaDone, 1u);
+    if (done == gridDim.x - 1) {
+      a.scratch[kNaDone] = 0u;
+      a.scratch[kNaEpoch] = s_epoch;
+      if (a.device_status)
+        *a.device_status = ld_volatile(a.scratch + kNaFailed) == s_epoch ? (int)PL_ERR_TIMEOUT : (int)PL_OK;
+      __threadfence();
+    }
+  }
+}
+
+template <typename T>
+const void* na_kernel(int world) {
+  if (world == 8) return (const void*)noalloc_kernel<T, 8>;
+  return (const void*)noalloc_kernel<T, 0>;
+}
+
+struct NaDevice {
+  uint32_t* scratch = nullptr;
+  int sm_count = 0;
+};
+
+std::mutex g_na_mu;
+NaDevice g_na_dev[kNaMaxDevices];
+
+// First call on a device: find the array's device address (host code only
+// holds a stand-in for it), zero it on the stream, and note the SM count.
+purlin_status na_setup(int dev, cudaStream_t stream, NaDevice* out) {
+  std::lock_guard<std::mutex> lock(g_na_mu);
+  NaDevice& d = g_na_dev[dev];
+  if (!d.scratch) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+      (void)cudaGetLastError();
+      return PL_ERR_CUDA;
+    }
+    if (cudaMemsetAsync(p, 0, sizeof(g_noalloc_scratch), stream) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return PL_ERR_CUDA;
+    }
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) {
+      (void)cudaGetLastError();
+      return PL_ERR_CUDA;
+    }
+    d.sm_count = sms;
+    d.scratch = (uint32_t*)p;
+  }
+  *out = d;
+  return PL_OK;
+}
+
+}  // namespace
+}  // namespace pl
+
+extern "C" purlin_status purlin_all_reduce_noalloc(int world, const void* const* src, void* const* dst,
+                                                   size_t bytes_per_rank, purlin_dtype dtype, int* device_status,
+                                                   purlin_stream_t stream) {
+  using namespace pl;
+  if (world < 1 || world > kMaxWorld || !src || !dst) return PL_ERR_INVALID_ARG;
+  if (dtype != PL_F32 && dtype != PL_BF16) return PL_ERR_UNSUPPORTED;
+  const uint64_t E = (uint64_t)elem_size(dtype);
+  for (int r = 0; r < world; ++r) {
+    if (!src[r] || !dst[r]) return PL_ERR_INVALID_ARG;
+    if (((uintptr_t)src[r] | (uintptr_t)dst[r]) % E) return PL_ERR_ALIGNMENT;
+  }
+  if (bytes_per_rank % E) return PL_ERR_ALIGNMENT;
+  // destinations disjoint from each other and from every source but their own (in place)
+  const uintptr_t S = bytes_per_rank;
+  for (int i = 0; i < world; ++i) {
+    const uintptr_t d0 = (uintptr_t)dst[i], d1 = d0 + S;
+    for (int j = 0; j < world; ++j) {
+      const uintptr_t s0 = (uintptr_t)src[j], s1 = s0 + S;
+      if (S && d0 < s1 && s0 < d1 && !(i == j && s0 == d0)) return PL_ERR_INVALID_ARG;
+      if (j > i) {
+        const uintptr_t e0 = (uintptr_t)dst[j], e1 = e0 + S;
+        if (S && d0 < e1 && e0 < d1) return PL_ERR_INVALID_ARG;
+      }
+    }
+  }
+  const uint64_t n = bytes_per_rank / E;
+  const uint64_t q = n / (uint64_t)world, rem = n % (uint64_t)world;
+  const uint64_t largest = (q + (rem ? 1 : 0)) * E;
+  const uint64_t tmax = (largest + kNaTile - 1) / kNaTile;
+  // the fixed flag array bounds the size: world * tmax tiles of 64 KiB
+  if ((uint64_t)world * tmax > (uint64_t)kNaMaxFlags) return PL_ERR_WORKSPACE;
+  if (bytes_per_rank == 0) return PL_OK;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNaMaxDevices) {
+    (void)cudaGetLastError();
+    return PL_ERR_CUDA;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  NaDevice d;
+  if (purlin_status st = na_setup(dev, s, &d)) return st;
+
+  const void* fn = dtype == PL_F32 ? na_kernel<float>(world) : na_kernel<bf16_tag>(world);
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kNaThreads, 0) != cudaSuccess || occ < 1) {
+    (void)cudaGetLastError();
+    return PL_ERR_LAUNCH;
+  }
+  NaArgs a = {};
+  uint32_t same = 1;
+  for (int r = 0; r < world; ++r) {
+    a.in[r] = (const char*)src[r];
+    a.out[r] = (char*)dst[r];
+    if ((((uintptr_t)dst[r]) & 15u) != (((uintptr_t)dst[0]) & 15u)) same = 0;
+  }
+  const int ctas = std::min(occ, 2) * d.sm_count;
+  a.scratch = d.scratch;
+  a.device_status = device_status;
+  a.timeout_ns = 2000000000ull;
+  a.q = q;
+  a.rem = rem;
+  a.elem = (uint32_t)E;
+  a.world = (uint32_t)world;
+  a.tmax = (uint32_t)tmax;
+  a.lag = (uint32_t)std::max<uint64_t>(1, ((uint64_t)ctas + 2ull * world - 1) / (2ull * world));
+  a.slots = (uint32_t)((tmax + a.lag) * 2ull * (uint64_t)world);
+  a.dst_coaligned = same;
+  const int grid = (int)std::min<uint64_t>((uint64_t)ctas, a.slots);
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kNaThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // the CTAs wait on each other: all must be resident
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&a};
+  if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return PL_ERR_LAUNCH;
+  }
+  return PL_OK;
+}

@@ -92,6 +92,7 @@ _SIGNATURES = {
     "purlin_set_wait_timeout_ns": (_i, [_vp, ctypes.c_uint64]),
     "purlin_debug_drop_notify": (_i, [_vp, ctypes.c_longlong]),
     "purlin_query": (_i, [_vp, ctypes.POINTER(_i), ctypes.POINTER(_i), ctypes.POINTER(_i)]),
+    "purlin_all_reduce_noalloc": (_i, [_i, _PP, _PP, _sz, _i, _vp, _vp]),
     "purlin_plan_describe": (_i, [_i, _i, _i, _SZP, ctypes.POINTER(ctypes.c_uint64),
                                   ctypes.POINTER(ctypes.c_uint64), _i, ctypes.POINTER(purlin_tune),
                                   ctypes.POINTER(purlin_item), _sz, _SZP, ctypes.POINTER(_i),
@@ -215,6 +216,12 @@ def purlin_atom_copy(h, src, dst, nbytes, stream=None) -> int:
 def purlin_atom_reduce(h, src, dst, nbytes, dtype, stream=None) -> int:
     return load().purlin_atom_reduce(h, _ptr_array(src), len(src), _ptr_array(dst), len(dst), nbytes, dtype,
                                      _stream(stream))
+
+
+def purlin_all_reduce_noalloc(world, src, dst, bytes_per_rank, dtype, device_status=None, stream=None) -> int:
+    """Allocation-free AllReduce (no handle); device_status: device int pointer or None."""
+    return load().purlin_all_reduce_noalloc(world, _ptr_array(src), _ptr_array(dst), bytes_per_rank, dtype,
+                                            _addr(device_status) or None, _stream(stream))
 
 
 def purlin_status_get(h, stream=None):

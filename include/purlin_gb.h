@@ -238,6 +238,34 @@ purlin_status purlin_debug_drop_notify(purlin_handle h, long long item);
  * and the largest number of CTAs of the reduce kernel resident per SM. */
 purlin_status purlin_query(purlin_handle h, int* sm_count, int* arch, int* max_ctas_per_sm);
 
+/* ------------------------------------------------- allocation-free variant */
+
+/* AllReduce (two-shot layout, same results as purlin_all_reduce: the
+ * ascending-rank binary32 fold, bit for bit) for callers that must not
+ * allocate device memory once running -- a runtime whose memory is fixed at
+ * start-up, a plug-in that has to stay inside its host framework's memory
+ * pool, code that cannot take the device-wide synchronisation cudaMalloc /
+ * cudaFree may cause.  The source pages have no counterpart to this call.
+ *
+ * It needs no handle and calls no allocating routine.  Its scratch (SNAC
+ * flags and control words, about 64 KiB) is a static array in the library,
+ * present on every GPU that loads it until the process exits.  The first call
+ * on a device looks up that array's device address and zeroes it on `stream`;
+ * make that first call before any stream capture.  Every call on a device
+ * shares the array: calls that overlap on the GPU (unordered streams) race
+ * and must not be made; calls ordered on one stream are fine.
+ *
+ * world in [1, PURLIN_MAX_WORLD]; src / dst as for purlin_all_reduce (in place
+ * allowed).  Size limit: world * ceil(largest rank share / 64 KiB) <= 16384
+ * tiles, where a rank share is bytes_per_rank / world rounded up to whole
+ * elements -- about 1 GiB per rank; larger sizes return PL_ERR_WORKSPACE and
+ * launch nothing.  device_status: NULL, or device memory the caller owns that
+ * receives PL_OK or PL_ERR_TIMEOUT (a SNAC wait gave up after 2 s) when the
+ * kernel ends.  Asynchronous on `stream`. */
+purlin_status purlin_all_reduce_noalloc(int world, const void* const* src, void* const* dst,
+                                        size_t bytes_per_rank, purlin_dtype dtype, int* device_status,
+                                        purlin_stream_t stream);
+
 /* ------------------------------------------------------- host-only plans */
 
 /* The plan a call would run, computed on the host with no GPU: the layout
