@@ -189,20 +189,22 @@ purlin_status get_plan(purlin_ctx* h, int coll, int world, int dtype, const uint
   d->threads = d->plan.tune.threads;
   if (d->plan.tune.path == pl::kPathBulk) {
     // ring of `stages` slots; a reduce slot holds nsrc input tiles and one output tile
-    const int tiles = d->plan.nsrc > 1 ? d->plan.nsrc + 1 : 1;
+    // (a copy slot holds a 16-byte-aligned source window of chunk + 16 bytes
+    // and an output tile, for sources that are not 16-byte aligned)
+    const int tiles = d->plan.nsrc > 1 ? d->plan.nsrc + 1 : 2;
     const int stages = d->plan.tune.stages;
     int64_t ch = d->plan.tune.chunk_bytes;
-    const int64_t fit = kMaxDynSmem / (int64_t)(stages * tiles);
+    const int64_t fit = (kMaxDynSmem / stages - 16) / tiles;
     if (ch > fit) ch = fit;
     if (ch > (1 << 20) / tiles) ch = (1 << 20) / tiles;  // mbarrier transaction count stays below 2^20
     ch &= ~(int64_t)15;
     if (ch < 16) return PL_ERR_INVALID_ARG;
     d->ring_chunk = (uint32_t)ch;
-    d->smem = (int)(stages * tiles * ch);
+    d->smem = (int)(stages * (tiles * ch + 16));
     cudaError_t e = cudaFuncSetAttribute(d->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, d->smem);
     if (e != cudaSuccess) return cuda_fail(e);
   }
-  if (d->plan.strided) {
+  if (d->plan.sync) {
     // CTAs of this plan wait on each other: all of them must be resident.
     int occ = 0;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, d->fn, d->threads, d->smem);
@@ -266,6 +268,7 @@ purlin_status run(purlin_ctx* h, int coll, int world, int dtype, const uint64_t*
   a.cta_begin = d->d_cta;
   a.n_items = (uint32_t)d->plan.items.size();
   a.strided = d->plan.strided ? 1u : 0u;
+  a.sync = d->plan.sync ? 1u : 0u;
   a.flags = h->flags;
   a.ctl = h->ctl;
   a.timeout_ns = h->timeout_ns;
@@ -283,7 +286,7 @@ purlin_status run(purlin_ctx* h, int coll, int world, int dtype, const uint64_t*
   cfg.dynamicSmemBytes = (size_t)d->smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  if (d->plan.strided) {
+  if (d->plan.sync) {
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;

@@ -21,7 +21,8 @@ struct KArgs {
   const Item* items;
   const uint32_t* cta_begin;  // contiguous assignment (nullptr when strided)
   uint32_t n_items;
-  uint32_t strided;           // item i on CTA i % grid; also marks plans with flags
+  uint32_t strided;           // item i on CTA i % grid (else contiguous ranges)
+  uint32_t sync;              // the plan has SNAC flags: epoch, status and done counter in use
   uint32_t* flags;
   uint32_t* ctl;              // status, epoch, done counter
   unsigned long long timeout_ns;

@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(512, 2) snac_kernel(const __grid_constant__ KA
     end = a.cta_begin[blockIdx.x + 1];
     step = 1;
   }
-  if (threadIdx.x == 0) s_epoch = a.strided ? ld_volatile(&a.ctl[kCtlEpoch]) + 1u : 0u;
+  if (threadIdx.x == 0) s_epoch = a.sync ? ld_volatile(&a.ctl[kCtlEpoch]) + 1u : 0u;
 
   // Thread 0 keeps the next item in registers so its load overlaps the current one.
   Item next;
@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(512, 2) snac_kernel(const __grid_constant__ KA
       s_notify = it.notify;
       int ok = 1;
       if (it.wait) ok = consume_wait(a, a.flags + (it.wait - 1), s_epoch);
-      if (a.strided && ok && ld_volatile(&a.ctl[kCtlStatus]) != 0) ok = 0;
+      if (a.sync && ok && ld_volatile(&a.ctl[kCtlStatus]) != 0) ok = 0;
       s_ok = ok;
     }
     __syncthreads();
@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(512, 2) snac_kernel(const __grid_constant__ KA
       st_release(a.flags + (s_notify - 1), s_epoch);
     }
   }
-  if (a.strided) {
+  if (a.sync) {
     // The last CTA to finish publishes the launch's epoch for the next one.
     __syncthreads();
     if (threadIdx.x == 0) {

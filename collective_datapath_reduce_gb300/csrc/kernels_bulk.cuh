@@ -153,6 +153,73 @@ __device__ void bulk_copy_body(BulkRing& R, char* ring, int stages, uint32_t ch,
   R.chunk = g0 + (uint32_t)n;
 }
 
+// Copy whose destinations are 16-byte aligned but whose source sits m bytes
+// (1..15) past a 16-byte boundary.  All threads.  Chunk k of the destination
+// needs source bytes [k*ch, k*ch + len) = the aligned window starting at
+// base + k*ch of round_up(m + len, 16) bytes; the window is loaded with one
+// bulk copy (it only spans granules that hold bytes of the source range),
+// every thread cuts its destination vectors out of it with funnel shifts into
+// the slot's output tile, and the leader bulk-stores the tile.  Slot layout:
+// window of ch + 16 bytes, then the output tile of ch bytes.
+__device__ void bulk_copy_shifted_body(BulkRing& R, char* ring, int stages, uint32_t ch, const char* src,
+                                       char* const* dst, int nd, uint64_t bytes, unsigned long long limit_ns) {
+  const uint32_t m = (uint32_t)((uintptr_t)src & 15u);
+  const char* base = src - m;
+  const size_t slot = (size_t)2 * ch + 16;
+  const uint64_t n = (bytes + ch - 1) / ch;
+  const uint32_t g0 = R.chunk;
+  const bool leader = threadIdx.x == 0;
+  auto chunk_len = [&](uint64_t k) -> uint32_t {
+    const uint64_t off = k * ch;
+    return (uint32_t)((bytes - off) < ch ? (bytes - off) : ch);
+  };
+  auto issue_load = [&](uint64_t k) {
+    const uint32_t s = (g0 + (uint32_t)k) % (uint32_t)stages;
+    const uint32_t win = (m + chunk_len(k) + 15u) & ~15u;
+    mbar_expect_tx(&R.full[s], win);
+    bulk_load(ring + s * slot, base + k * ch, win, &R.full[s]);
+  };
+  if (leader) {
+    const uint64_t pre = n < (uint64_t)stages ? n : (uint64_t)stages;
+    for (uint64_t k = 0; k < pre; ++k) issue_load(k);
+  }
+  uint64_t k = 0;
+  for (; k < n; ++k) {
+    const uint32_t g = g0 + (uint32_t)k;
+    const uint32_t s = g % (uint32_t)stages;
+    const bool ok = mbar_wait(&R.full[s], (g / (uint32_t)stages) & 1u, limit_ns);
+    if (leader) bulk_wait_read_dyn(stages - 1);
+    if (__syncthreads_or(!ok)) {
+      if (leader) R.failed = 1;
+      break;
+    }
+    const uint32_t len = chunk_len(k);
+    const uint4* win = reinterpret_cast<const uint4*>(ring + s * slot);
+    uint4* otile = reinterpret_cast<uint4*>(ring + s * slot + ch + 16);
+    for (uint32_t v = threadIdx.x; v < len / 16; v += blockDim.x) otile[v] = window16(win[v], win[v + 1], m);
+    fence_async_shared();
+    __syncthreads();
+    if (leader) {
+      for (int j = 0; j < nd; ++j) bulk_store(dst[j] + k * ch, otile, len);
+      bulk_commit();
+      if (k + (uint64_t)stages < n) issue_load(k + (uint64_t)stages);
+    }
+  }
+  if (leader) {
+    if (R.failed) {
+      const uint64_t issued = (k + (uint64_t)stages < n) ? k + (uint64_t)stages : n;
+      for (uint64_t j = k + 1; j < issued; ++j) {
+        const uint32_t gj = g0 + (uint32_t)j;
+        mbar_wait(&R.full[gj % (uint32_t)stages], (gj / (uint32_t)stages) & 1u, limit_ns);
+      }
+      R.chunk = g0 + (uint32_t)issued;
+    } else {
+      R.chunk = g0 + (uint32_t)n;
+    }
+  }
+  __syncthreads();
+}
+
 // Reduce of the aligned body [0, bytes) of one item.  All threads.
 // Slot layout: NSRC input tiles of `ch` bytes, then one output tile.
 template <typename T, int NS>
@@ -250,6 +317,7 @@ __global__ void __launch_bounds__(512, 1) bulk_kernel(const __grid_constant__ KA
   __shared__ BulkRing R;
   __shared__ const char* s_src[kMaxWorld];
   __shared__ char* s_dst[kMaxWorld];
+  __shared__ char* s_dst_body[kMaxWorld];
   __shared__ uint64_t s_len;
   __shared__ int s_ns, s_nd, s_ok, s_aligned;
   __shared__ uint32_t s_notify, s_epoch;
@@ -260,7 +328,7 @@ __global__ void __launch_bounds__(512, 1) bulk_kernel(const __grid_constant__ KA
     for (int i = 0; i < stages; ++i) mbar_init(&R.full[i], 1);
     R.chunk = 0;
     R.failed = 0;
-    s_epoch = a.strided ? ld_volatile(&a.ctl[kCtlEpoch]) + 1u : 0u;
+    s_epoch = a.sync ? ld_volatile(&a.ctl[kCtlEpoch]) + 1u : 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_async_shared();
   }
@@ -306,15 +374,41 @@ __global__ void __launch_bounds__(512, 1) bulk_kernel(const __grid_constant__ KA
         ok = consume_wait(a, a.flags + (it.wait - 1), s_epoch);
         fence_async_global();  // the bulk loads below must see what the producer released
       }
-      if (a.strided && ok && ld_volatile(&a.ctl[kCtlStatus]) != 0) ok = 0;
+      if (a.sync && ok && ld_volatile(&a.ctl[kCtlStatus]) != 0) ok = 0;
       s_ok = ok && !R.failed;
     }
     __syncthreads();
     if (!s_ok) break;
     const uint64_t len = s_len;
     const int ns = s_ns, nd = s_nd;
-    if (!s_aligned) {
-      // unaligned items take the register path
+    if (!s_aligned && ns == 1) {
+      // Copy with misaligned addresses: bytes up to the destinations' 16-byte
+      // boundary and the ragged end go through registers, the body through the
+      // shifted bulk pipeline.  Loads are L2 loads: the source may be another
+      // CTA's output.
+      const uint32_t rd = (uint32_t)((uintptr_t)s_dst[0] & 15u);
+      const uint64_t head = ((16u - rd) & 15u) < len ? ((16u - rd) & 15u) : len;
+      const uint64_t body = (len - head) & ~(uint64_t)15;
+      for (uint64_t k = threadIdx.x; k < head; k += blockDim.x) {
+        const uint8_t b = ld_byte<true>(s_src[0] + k);
+        for (int j = 0; j < nd; ++j) s_dst[j][k] = (char)b;
+      }
+      for (uint64_t k = head + body + threadIdx.x; k < len; k += blockDim.x) {
+        const uint8_t b = ld_byte<true>(s_src[0] + k);
+        for (int j = 0; j < nd; ++j) s_dst[j][k] = (char)b;
+      }
+      if (body) {
+        if (threadIdx.x < kMaxWorld) s_dst_body[threadIdx.x] = threadIdx.x < (unsigned)nd ? s_dst[threadIdx.x] + head : nullptr;
+        __syncthreads();
+        const char* sb = s_src[0] + head;
+        if (((uintptr_t)sb & 15u) == 0) {
+          if (threadIdx.x == 0) bulk_copy_body(R, dyn_smem, stages, ch, sb, s_dst_body, nd, body, kBulkWaitNs);
+        } else {
+          bulk_copy_shifted_body(R, dyn_smem, stages, ch, sb, s_dst_body, nd, body, kBulkWaitNs);
+        }
+      }
+    } else if (!s_aligned) {
+      // misaligned reductions take the register path
       if constexpr (std::is_same<T, void>::value) {
         copy_atom<false, 4, false>(s_src[0], s_dst, nd, len);
       } else {
@@ -356,7 +450,7 @@ __global__ void __launch_bounds__(512, 1) bulk_kernel(const __grid_constant__ KA
     }
   }
   if (threadIdx.x == 0) bulk_wait_all();  // shared memory stays valid until every store has read it
-  if (a.strided) {
+  if (a.sync) {
     __syncthreads();
     if (threadIdx.x == 0) {
       __threadfence();

@@ -190,6 +190,7 @@ Tune tune_merge(const Tune& b, const Tune& o) {
   if (o.stages) t.stages = o.stages;
   if (o.store_hint) t.store_hint = o.store_hint;
   if (o.min_cta_bytes) t.min_cta_bytes = o.min_cta_bytes;
+  if (o.interleave_bytes) t.interleave_bytes = o.interleave_bytes;
   return t;
 }
 
@@ -203,6 +204,8 @@ static int validate_tune(const Tune& t) {
   if (t.stages < 2 || t.stages > 8) return PL_ERR_INVALID_ARG;
   if (t.store_hint < 1 || t.store_hint > 2) return PL_ERR_INVALID_ARG;
   if (t.min_cta_bytes < 16) return PL_ERR_INVALID_ARG;
+  if (t.interleave_bytes < 0 || (t.interleave_bytes && (t.interleave_bytes < 512 || t.interleave_bytes % 512)))
+    return PL_ERR_INVALID_ARG;
   return PL_OK;
 }
 
@@ -416,12 +419,22 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
   const uint64_t gcap = (uint64_t)p.tune.ctas_per_sm * (uint64_t)sm_count;
   if (sync) {
     p.strided = true;
+    p.sync = true;
     p.n_flags = (int)n_flags;
     const uint64_t n = pieces.size();
     p.grid = (int)std::max<uint64_t>(1, std::min<uint64_t>(gcap, n));
     p.items.reserve(n);
     for (const Piece& q : pieces)
       p.items.push_back(Item{q.src_off, q.dst_off, q.len, q.src_mask, q.dst_mask, q.wait, q.notify});
+  } else if (p.tune.interleave_bytes > 0) {
+    // Tiles of interleave_bytes dealt round-robin: at any moment the CTAs work
+    // on neighbouring tiles instead of one contiguous share each.
+    p.strided = true;
+    const uint64_t T = (uint64_t)p.tune.interleave_bytes;
+    for (const Piece& q : pieces)
+      for (uint64_t a = 0; a < q.len; a += T)
+        p.items.push_back(Item{q.src_off + a, q.dst_off + a, std::min(T, q.len - a), q.src_mask, q.dst_mask, 0, 0});
+    p.grid = (int)std::max<uint64_t>(1, std::min<uint64_t>(gcap, p.items.size()));
   } else {
     uint64_t W = 0;
     for (const Piece& q : pieces) W += q.len;

@@ -63,6 +63,7 @@ struct Tune {
   int stages = 0;
   int store_hint = 0;
   int min_cta_bytes = 0;
+  int interleave_bytes = 0;  // > 0: tiles of this size dealt round-robin to the CTAs
 };
 
 struct Plan {
@@ -73,6 +74,7 @@ struct Plan {
   std::vector<Item> items;   // global order
   std::vector<uint32_t> cta_begin;  // contiguous assignment: grid + 1 entries
   bool strided = false;      // item i runs on CTA i % grid, in increasing i
+  bool sync = false;         // items wait on / notify SNAC flags (CTAs must be co-resident)
   int grid = 0;
   int n_flags = 0;           // SNAC flags used (two-shot layout)
   uint64_t in_bytes[kMaxWorld] = {};   // bytes each input must hold

@@ -97,13 +97,16 @@ typedef enum {
 typedef struct {
   int layout;       /* purlin_layout; AllReduce only */
   int ctas_per_sm;  /* persistent CTAs per SM (grid = ctas_per_sm x SMs, capped by work) */
-  int threads;      /* threads per CTA: a multiple of 32 in [64, 1024] */
+  int threads;      /* threads per CTA: a multiple of 32 in [64, 512] */
   int unroll;       /* 16-byte vectors in flight per thread per source, 1..8 */
   int path;         /* 1 = register path, 2 = TMA bulk pipeline through shared memory */
   int chunk_bytes;  /* TMA stage size per source, or SNAC tile size for the two-shot layout */
   int stages;       /* TMA pipeline depth, 2..8 */
   int store_hint;   /* 1 = default write-back stores, 2 = streaming (evict-first) stores */
   int min_cta_bytes;/* fewest work bytes given to one CTA before the grid shrinks */
+  int interleave_bytes; /* 0: each CTA takes one contiguous share of the work; a multiple
+                           of 512: the work is cut into tiles of this size dealt
+                           round-robin to the CTAs */
 } purlin_tune;
 
 /* One work item of a plan, as purlin_plan_describe reports it. */

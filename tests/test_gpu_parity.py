@@ -581,3 +581,39 @@ def test_v_variants_accept_null_for_empty_ranks():
         assert np.array_equal(dst.read(d)[:want[d].size], want[d])
     assert P.purlin_all_gather_v(h.h, [0, 0, 0], dst.ptrs(), [1, 0, 0], stream()) == P.PL_ERR_INVALID_ARG
     assert h.close() == P.PL_OK
+
+
+@pytest.mark.parametrize("path", [P.PATH_REGISTER, P.PATH_BULK])
+def test_interleaved_tiles(path):
+    tune = {"interleave_bytes": 16384, "path": path, "stages": 3, "chunk_bytes": 8192}
+    for dtype in ("f32", "bf16"):
+        ins, outs = run_all_reduce(8, dtype, (1 << 20) + 24, P.PL_LAYOUT_ONE_SHOT, tune=tune)
+        want = oracle.all_reduce(ins, dtype)
+        for r in range(8):
+            assert np.array_equal(bits(outs[r]), bits(want[r]))
+    world = 8
+    C, c = inputs.w5_counts(world, max_count=30000, seed=4)
+    a2av_in, agv_in = inputs.w5_payloads(C, c, seed=4)
+    outs = run_copy("a2av", world, a2av_in, [int(v) * 2 for v in C.reshape(-1)],
+                    [int(C[:, d].sum()) * 2 for d in range(world)], tune=tune)
+    want = oracle.all_to_all_v(a2av_in, C)
+    for r in range(world):
+        assert np.array_equal(outs[r].view(np.uint16), want[r])
+    outs = run_copy("agv", world, agv_in, [int(v) * 2 for v in c], [int(c.sum()) * 2] * world, tune=tune)
+    want = oracle.all_gather_v(agv_in, [int(v) for v in c])
+    for r in range(world):
+        assert np.array_equal(outs[r].view(np.uint16), want[r])
+
+
+@pytest.mark.parametrize("smis,dmis", [([2, 6, 10, 14], [0, 0, 0, 0]), ([0, 4, 8, 12], [2, 2, 2, 2]),
+                                       ([1, 3, 5, 7], [9, 9, 9, 9])])
+def test_bulk_shifted_copies(smis, dmis):
+    """Sources misaligned against 16-byte destinations: the shifted bulk pipeline."""
+    tune = {"path": P.PATH_BULK, "stages": 3, "chunk_bytes": 4096}
+    world = 4
+    for S in (17, 4096 + 2, 100000 + 6, (1 << 20) + 10):
+        ins = [RNG.integers(0, 256, size=S, dtype=np.uint8) for _ in range(world)]
+        outs = run_copy("ag", world, ins, S, [world * S] * world, smis, dmis, tune=tune)
+        want = oracle.all_gather(ins)
+        for r in range(world):
+            assert np.array_equal(outs[r], want[r]), (S, r)

@@ -187,3 +187,33 @@ def test_full_size_plans_are_balanced():
         assert per.max() - per.min() <= 1024, (coll, per.min(), per.max())
         for it in items:   # every CTA share starts on a 512-byte boundary of its piece
             assert it["src_off"] % 512 == 0 and it["dst_off"] % 512 == 0
+
+
+@pytest.mark.parametrize("interleave", [512, 4096, 65536])
+def test_interleaved_plans(interleave):
+    """Tiles dealt round-robin cover every output byte once and match the oracle."""
+    tune = {"interleave_bytes": interleave}
+    world = 8
+    for dtype in ("f32", "bf16"):
+        E = ESZ[dtype]
+        n = 70001
+        ins = [_draw(dtype, n) for _ in range(world)]
+        items, grid, nflags = _describe(P.PL_COLL_ALL_REDUCE, world, DT[dtype], [n * E], sm=7, tune=tune)
+        assert nflags == 0
+        for i, it in enumerate(items):
+            assert it["cta"] == i % grid and it["len"] <= interleave
+        outs = [np.zeros(n * E, np.uint8) for _ in range(world)]
+        run_items(items, [_bytes(x) for x in ins], outs, dtype)
+        want = oracle.all_reduce(ins, dtype)
+        for r in range(world):
+            assert np.array_equal(outs[r], _bytes(want[r]))
+    C = RNG.integers(0, 3000, size=(world, world))
+    ins = [RNG.integers(0, 256, size=int(C[s].sum()), dtype=np.uint8) for s in range(world)]
+    items, _, _ = _describe(P.PL_COLL_ALL_TO_ALL_V, world, P.PL_U8, C.reshape(-1).tolist(), sm=3, tune=tune)
+    outs = [np.zeros(int(C[:, d].sum()), np.uint8) for d in range(world)]
+    run_items(items, ins, outs, "u8")
+    want = oracle.all_to_all_v(ins, C)
+    for r in range(world):
+        assert np.array_equal(outs[r], want[r])
+    st, *_ = P.purlin_plan_describe(P.PL_COLL_ALL_GATHER, 2, P.PL_U8, [64], tune={"interleave_bytes": 100})
+    assert st == P.PL_ERR_INVALID_ARG
