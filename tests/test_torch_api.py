@@ -1,0 +1,70 @@
+"""The torch-tensor front end: argument checks on the CPU, results on the GPU."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from collective_datapath_reduce_gb300 import inputs
+from collective_datapath_reduce_gb300 import torch_api as purlin
+
+
+def test_rejects_host_tensors_without_touching_the_library():
+    h = purlin.Handle(raw=None, world=2, device=torch.device("cpu"))
+    xs = [torch.zeros(4), torch.zeros(4)]
+    with pytest.raises(ValueError):
+        purlin.all_reduce(xs, xs, h)
+    with pytest.raises(ValueError):
+        purlin.all_gather(xs[:1], xs[:1], h)
+
+
+@pytest.mark.gpu
+def test_torch_front_end_matches_oracle():
+    dev = torch.device("cuda", 0)
+    world, n = 4, 100003
+    rng = np.random.default_rng(5)
+    h = purlin.initialize(world, dev)
+    try:
+        x = [inputs.to_bf16_bits(rng.standard_normal(n).astype(np.float32)) for _ in range(world)]
+        xs = [torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev) for a in x]
+        outs = [torch.empty_like(t) for t in xs]
+        purlin.all_reduce(xs, outs, h, reduction_mode=purlin.ReductionMode.DETERMINISTIC)
+        torch.cuda.synchronize()
+        want = oracle.all_reduce(x, "bf16")
+        for r in range(world):
+            assert np.array_equal(outs[r].view(torch.int16).cpu().numpy().view(np.uint16), want[r])
+        purlin.all_reduce(xs, xs, h)   # in place
+        torch.cuda.synchronize()
+        for r in range(world):
+            assert np.array_equal(xs[r].view(torch.int16).cpu().numpy().view(np.uint16), want[r])
+        f = [rng.standard_normal(world * 1000).astype(np.float32) for _ in range(world)]
+        fs = [torch.from_numpy(a).to(dev) for a in f]
+        rs = [torch.empty(1000, device=dev) for _ in range(world)]
+        purlin.reduce_scatter(fs, rs, h)
+        ag = [torch.empty(world * 1000, device=dev) for _ in range(world)]
+        purlin.all_gather(rs, ag, h)
+        aa = [torch.empty(world * 1000, device=dev) for _ in range(world)]
+        purlin.all_to_all(fs, aa, h)
+        torch.cuda.synchronize()
+        want_rs = oracle.reduce_scatter(f, "f32")
+        want_ag = oracle.all_gather(want_rs)
+        want_aa = oracle.all_to_all(f)
+        for r in range(world):
+            assert np.array_equal(rs[r].cpu().numpy().view(np.uint32), want_rs[r].view(np.uint32))
+            assert np.array_equal(ag[r].cpu().numpy().view(np.uint32), want_ag[r].view(np.uint32))
+            assert np.array_equal(aa[r].cpu().numpy().view(np.uint32), want_aa[r].view(np.uint32))
+        counts = [[3, 0, 5, 1], [2, 2, 2, 2], [0, 0, 0, 7], [1, 1, 0, 0]]
+        send = [rng.standard_normal(sum(row)).astype(np.float32) for row in counts]
+        ss = [torch.from_numpy(a).to(dev) for a in send]
+        rr = [torch.empty(sum(counts[s][d] for s in range(world)), device=dev) for d in range(world)]
+        purlin.all_to_all_v(ss, rr, counts, h)
+        agv = [torch.empty(sum(len(a) for a in send), device=dev) for _ in range(world)]
+        purlin.all_gather_v(ss, agv, h)
+        torch.cuda.synchronize()
+        want = oracle.all_to_all_v(send, counts)
+        want_g = oracle.all_gather_v(send, [len(a) for a in send])
+        for r in range(world):
+            assert np.array_equal(rr[r].cpu().numpy(), want[r])
+            assert np.array_equal(agv[r].cpu().numpy(), want_g[r])
+    finally:
+        purlin.finalize(h)
