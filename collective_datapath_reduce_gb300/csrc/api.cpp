@@ -60,6 +60,8 @@ struct purlin_ctx {
   bool has_over = false;
   unsigned long long timeout_ns = kDefaultTimeoutNs;
   long long drop_notify = -1;
+  unsigned long long* trace = nullptr;  // caller's trace buffer, or nullptr
+  uint32_t trace_cap = 0;
   bool finalized = false;
 };
 
@@ -201,7 +203,9 @@ purlin_status get_plan(purlin_ctx* h, int coll, int world, int dtype, const uint
     if (ch < 16) return PL_ERR_INVALID_ARG;
     d->ring_chunk = (uint32_t)ch;
     d->smem = (int)(stages * (tiles * ch + 16));
-    cudaError_t e = cudaFuncSetAttribute(d->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, d->smem);
+    // The limit is a property of the kernel function, shared by every plan that
+    // launches it: raise it to the largest ring any plan may use, never lower it.
+    cudaError_t e = cudaFuncSetAttribute(d->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   if (d->plan.sync) {
@@ -277,6 +281,8 @@ purlin_status run(purlin_ctx* h, int coll, int world, int dtype, const uint64_t*
   a.store_hint = d->plan.tune.store_hint;
   a.stages = d->plan.tune.stages;
   a.chunk_bytes = d->ring_chunk;
+  a.trace = h->trace;
+  a.trace_cap = h->trace_cap;
   h->drop_notify = -1;
 
   cudaLaunchConfig_t cfg;
@@ -660,6 +666,22 @@ purlin_status purlin_debug_drop_notify(purlin_handle h, long long item) {
   purlin_status st;
   if ((st = check_handle(h))) return st;
   h->drop_notify = item < 0 ? -1 : item;
+  return PL_OK;
+}
+
+purlin_status purlin_trace_enable(purlin_handle h, void* buffer, size_t buffer_bytes) {
+  purlin_status st;
+  if ((st = check_handle(h))) return st;
+  std::lock_guard<std::mutex> lock(h->mu);
+  if (!buffer) {
+    h->trace = nullptr;
+    h->trace_cap = 0;
+    return PL_OK;
+  }
+  if (((uintptr_t)buffer & 7u) || buffer_bytes < 8 + sizeof(pl::TraceRecord)) return PL_ERR_INVALID_ARG;
+  const size_t cap = (buffer_bytes - 8) / sizeof(pl::TraceRecord);
+  h->trace = (unsigned long long*)buffer;
+  h->trace_cap = (uint32_t)std::min<size_t>(cap, 0xFFFFFFFFu);
   return PL_OK;
 }
 

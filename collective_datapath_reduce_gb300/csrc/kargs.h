@@ -31,7 +31,21 @@ struct KArgs {
   int store_hint;             // 1 write-back, 2 streaming
   int stages;                 // bulk path: slots in the shared-memory ring
   uint32_t chunk_bytes;       // bulk path: bytes per source tile in a slot
+  unsigned long long* trace;  // trace buffer (header word + records), or nullptr
+  uint32_t trace_cap;         // records the trace buffer holds
 };
+
+// One trace record (32 bytes): which CTA ran which item, when, and how long it
+// waited for its SNAC flag.  The buffer starts with one 64-bit record count.
+struct TraceRecord {
+  unsigned long long t_start;  // %globaltimer when the item was picked up (ns)
+  unsigned long long t_end;    // when the CTA had issued the item's stores (and raised its flag)
+  uint32_t cta;
+  uint32_t item;
+  uint32_t wait_ns;            // time in the consume wait
+  uint32_t len_kib;            // item length in KiB (rounded down)
+};
+static_assert(sizeof(TraceRecord) == 32, "trace record layout");
 
 // Kernel entry points (device function addresses), by variant.  nullptr when
 // the variant is not built.

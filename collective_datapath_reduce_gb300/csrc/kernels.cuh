@@ -341,6 +341,22 @@ __device__ __forceinline__ bool consume_wait(const KArgs& a, const uint32_t* fla
   }
 }
 
+// Append one record to the trace buffer (thread 0).  Records past the
+// capacity are counted but not written.
+__device__ __forceinline__ void trace_put(const KArgs& a, unsigned long long t0, unsigned long long t1,
+                                          uint32_t item, uint32_t wait_ns, uint64_t len) {
+  const unsigned long long slot = atomicAdd(a.trace, 1ull);
+  if (slot < a.trace_cap) {
+    TraceRecord* r = reinterpret_cast<TraceRecord*>(a.trace + 1) + slot;
+    r->t_start = t0;
+    r->t_end = t1;
+    r->cta = blockIdx.x;
+    r->item = item;
+    r->wait_ns = wait_ns;
+    r->len_kib = (uint32_t)(len >> 10);
+  }
+}
+
 // T = void: copy-only kernel (AllGather, AllToAll and their V forms).
 // Otherwise items with one source are the consume-side copies of the
 // two-shot AllReduce, whose source another CTA produced in this launch.
@@ -363,7 +379,8 @@ __global__ void __launch_bounds__(512, 2) snac_kernel(const __grid_constant__ KA
   __shared__ char* s_dst[kMaxWorld];
   __shared__ uint64_t s_len;
   __shared__ int s_ns, s_nd, s_ok;
-  __shared__ uint32_t s_notify, s_epoch;
+  __shared__ uint32_t s_notify, s_epoch, s_wait_ns;
+  __shared__ unsigned long long s_t0;
 
   uint32_t begin, end, step;
   if (a.strided) {
@@ -395,7 +412,10 @@ __global__ void __launch_bounds__(512, 2) snac_kernel(const __grid_constant__ KA
       s_len = it.len;
       s_notify = it.notify;
       int ok = 1;
+      const unsigned long long t0 = a.trace ? globaltimer() : 0ull;
       if (it.wait) ok = consume_wait(a, a.flags + (it.wait - 1), s_epoch);
+      s_t0 = t0;
+      s_wait_ns = a.trace ? (uint32_t)min(globaltimer() - t0, 0xFFFFFFFFull) : 0u;
       if (a.sync && ok && ld_volatile(&a.ctl[kCtlStatus]) != 0) ok = 0;
       s_ok = ok;
     }
@@ -406,9 +426,12 @@ __global__ void __launch_bounds__(512, 2) snac_kernel(const __grid_constant__ KA
     else
       run_item<T, NS, U, false>(s_src, s_ns, s_dst, s_nd, s_len);
     __syncthreads();
-    if (threadIdx.x == 0 && s_notify && i + 1 != a.drop_notify) {
-      __threadfence();
-      st_release(a.flags + (s_notify - 1), s_epoch);
+    if (threadIdx.x == 0) {
+      if (s_notify && i + 1 != a.drop_notify) {
+        __threadfence();
+        st_release(a.flags + (s_notify - 1), s_epoch);
+      }
+      if (a.trace) trace_put(a, s_t0, globaltimer(), i, s_wait_ns, s_len);
     }
   }
   if (a.sync) {

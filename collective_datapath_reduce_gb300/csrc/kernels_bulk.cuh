@@ -320,7 +320,8 @@ __global__ void __launch_bounds__(512, 1) bulk_kernel(const __grid_constant__ KA
   __shared__ char* s_dst_body[kMaxWorld];
   __shared__ uint64_t s_len;
   __shared__ int s_ns, s_nd, s_ok, s_aligned;
-  __shared__ uint32_t s_notify, s_epoch;
+  __shared__ uint32_t s_notify, s_epoch, s_wait_ns;
+  __shared__ unsigned long long s_t0;
 
   const int stages = a.stages;
   const uint32_t ch = a.chunk_bytes;
@@ -370,10 +371,13 @@ __global__ void __launch_bounds__(512, 1) bulk_kernel(const __grid_constant__ KA
       s_notify = it.notify;
       s_aligned = (orr & 15u) == 0;
       int ok = 1;
+      const unsigned long long t0 = a.trace ? globaltimer() : 0ull;
       if (it.wait) {
         ok = consume_wait(a, a.flags + (it.wait - 1), s_epoch);
         fence_async_global();  // the bulk loads below must see what the producer released
       }
+      s_t0 = t0;
+      s_wait_ns = a.trace ? (uint32_t)min(globaltimer() - t0, 0xFFFFFFFFull) : 0u;
       if (a.sync && ok && ld_volatile(&a.ctl[kCtlStatus]) != 0) ok = 0;
       s_ok = ok && !R.failed;
     }
@@ -447,6 +451,7 @@ __global__ void __launch_bounds__(512, 1) bulk_kernel(const __grid_constant__ KA
         __threadfence();
         st_release(a.flags + (s_notify - 1), s_epoch);
       }
+      if (a.trace) trace_put(a, s_t0, globaltimer(), i, s_wait_ns, s_len);
     }
   }
   if (threadIdx.x == 0) bulk_wait_all();  // shared memory stays valid until every store has read it

@@ -95,11 +95,13 @@ size_t n_sizes(int coll, int world) {
   }
 }
 
-// Tuning table, from the sweep measured on a GB300 (152 SMs, HBM3e):
+// Tuning table, from the sweeps measured on a GB300 (152 SMs, HBM3e):
 // `bytes_per_rank` is the per-rank size the collective moves (for the V
 // variants, their total divided by the world).  Summary of what won:
-//   AllReduce   register path, 256 threads x 2 CTAs/SM (90% of the measured
-//               copy bandwidth at 8 x 64 MiB bf16); the fewest bytes per CTA
+//   AllReduce   register path, 256 threads x 2 CTAs/SM; from 32 MiB per rank
+//               16 KiB tiles dealt round-robin with evict-first stores (94% of
+//               the measured copy bandwidth at 8 x 64 MiB bf16, against 90%
+//               with one contiguous share per CTA); the fewest bytes per CTA
 //               stay at 512 so small calls spread over many CTAs.
 //   ReduceScatter  from 8 MiB per rank the TMA bulk ring (2 slots x 32 KiB
 //               per source) runs above the copy bandwidth: the traffic is
@@ -127,7 +129,18 @@ Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
     case kAtomReduce:
       t.unroll = world <= 4 ? 2 : 1;
       t.chunk_bytes = 64 * 1024;  // two-shot tile
-      if (S <= 4 * MiB) t.threads = 512;
+      if (S >= 32 * MiB) {
+        // 16 KiB tiles dealt round-robin with evict-first stores: all CTAs
+        // sweep neighbouring addresses of the 2N buffers together
+        t.interleave_bytes = 16 * 1024;
+        t.store_hint = 2;
+      } else if (S >= 8 * MiB) {
+        t.threads = 512;
+        t.interleave_bytes = (int)std::min<uint64_t>(128 * KiB, std::max<uint64_t>(16 * KiB, S / 128));
+        t.store_hint = 2;
+      } else {
+        t.threads = 512;
+      }
       break;
     case kReduceScatter:
     case kReduceScatterV:
@@ -149,7 +162,9 @@ Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
         t.path = kPathBulk;
         t.ctas_per_sm = 1;
         t.stages = 4;
-        t.chunk_bytes = 4 * 1024;
+        // AllGatherV pieces are mostly misaligned (shifted bulk copies), which
+        // amortise better over larger chunks
+        t.chunk_bytes = coll == kAllGatherV ? 32 * 1024 : 4 * 1024;
       } else if (S >= 256 * KiB) {
         t.threads = 512;
         t.min_cta_bytes = 2 * 1024;
@@ -426,24 +441,28 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
     p.items.reserve(n);
     for (const Piece& q : pieces)
       p.items.push_back(Item{q.src_off, q.dst_off, q.len, q.src_mask, q.dst_mask, q.wait, q.notify});
-  } else if (p.tune.interleave_bytes > 0) {
-    // Tiles of interleave_bytes dealt round-robin: at any moment the CTAs work
-    // on neighbouring tiles instead of one contiguous share each.
-    p.strided = true;
-    const uint64_t T = (uint64_t)p.tune.interleave_bytes;
-    for (const Piece& q : pieces)
-      for (uint64_t a = 0; a < q.len; a += T)
-        p.items.push_back(Item{q.src_off + a, q.dst_off + a, std::min(T, q.len - a), q.src_mask, q.dst_mask, 0, 0});
-    p.grid = (int)std::max<uint64_t>(1, std::min<uint64_t>(gcap, p.items.size()));
   } else {
+    // The concatenated piece space is cut into `nparts` near-equal parts at
+    // 512-byte granules of each piece.  Without interleaving nparts = grid and
+    // CTA c takes part c (one contiguous share).  With interleave_bytes = T,
+    // nparts = k * grid with parts of about T bytes, and CTA c takes parts
+    // c, c + grid, c + 2 grid, ... in that order: at any moment the CTAs work
+    // on neighbouring parts, and every CTA still gets the same number of bytes.
     uint64_t W = 0;
     for (const Piece& q : pieces) W += q.len;
     uint64_t G = std::max<uint64_t>(1, std::min<uint64_t>(gcap, ceil_div(W, (uint64_t)p.tune.min_cta_bytes)));
     G = std::min<uint64_t>(G, std::max<uint64_t>(1, W / kSplitGranule));
+    uint64_t k = 1;
+    if (p.tune.interleave_bytes > 0) {
+      const uint64_t T = (uint64_t)p.tune.interleave_bytes;
+      k = std::max<uint64_t>(1, (W + T * G / 2) / (T * G));
+      k = std::min<uint64_t>(k, std::max<uint64_t>(1, W / (kSplitGranule * G)));
+    }
+    const uint64_t nparts = k * G;
     p.grid = (int)G;
     std::vector<uint64_t> start(pieces.size() + 1, 0);
     for (size_t i = 0; i < pieces.size(); ++i) start[i + 1] = start[i] + pieces[i].len;
-    // boundary b of the concatenated space -> (piece, offset rounded down to 16)
+    // boundary b of the concatenated space -> (piece, offset rounded down to the granule)
     auto locate = [&](uint64_t b, size_t& pi, uint64_t& off) {
       if (b >= W) {
         pi = pieces.size();
@@ -453,27 +472,28 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
       pi = (size_t)(std::upper_bound(start.begin(), start.end(), b) - start.begin()) - 1;
       off = (b - start[pi]) & ~(kSplitGranule - 1);
     };
+    std::vector<std::vector<Item>> per_cta((size_t)G);
     size_t cp = 0;
     uint64_t co = 0;
-    p.cta_begin.push_back(0);
-    for (uint64_t c = 0; c < G; ++c) {
+    for (uint64_t j = 0; j < nparts; ++j) {
       size_t ep;
       uint64_t eo;
-      if (c + 1 == G) {
+      if (j + 1 == nparts) {
         ep = pieces.size();
         eo = 0;
       } else {
-        // exact integer share boundary: floor((c+1) * W / G) without overflow
-        const uint64_t b = (uint64_t)(((unsigned __int128)(c + 1) * W) / G);
+        // exact integer part boundary: floor((j+1) * W / nparts) without overflow
+        const uint64_t b = (uint64_t)(((unsigned __int128)(j + 1) * W) / nparts);
         locate(b, ep, eo);
       }
+      std::vector<Item>& dst = per_cta[(size_t)(j % G)];
       while (cp < ep || (cp == ep && co < eo)) {
         const Piece& q = pieces[cp];
         const uint64_t end = (cp == ep) ? eo : q.len;
         // items stay below 1 GiB so the Atoms can count 16-byte vectors in 32 bits
         for (uint64_t a = co; a < end; a += kMaxItemBytes) {
           const uint64_t l = std::min<uint64_t>(kMaxItemBytes, end - a);
-          p.items.push_back(Item{q.src_off + a, q.dst_off + a, l, q.src_mask, q.dst_mask, 0, 0});
+          dst.push_back(Item{q.src_off + a, q.dst_off + a, l, q.src_mask, q.dst_mask, 0, 0});
         }
         if (cp == ep) {
           co = eo;
@@ -482,6 +502,10 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
         ++cp;
         co = 0;
       }
+    }
+    p.cta_begin.push_back(0);
+    for (const auto& v : per_cta) {
+      p.items.insert(p.items.end(), v.begin(), v.end());
       p.cta_begin.push_back((uint32_t)p.items.size());
     }
   }

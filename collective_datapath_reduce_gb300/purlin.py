@@ -93,6 +93,7 @@ _SIGNATURES = {
     "purlin_debug_drop_notify": (_i, [_vp, ctypes.c_longlong]),
     "purlin_query": (_i, [_vp, ctypes.POINTER(_i), ctypes.POINTER(_i), ctypes.POINTER(_i)]),
     "purlin_all_reduce_noalloc": (_i, [_i, _PP, _PP, _sz, _i, _vp, _vp]),
+    "purlin_trace_enable": (_i, [_vp, _vp, _sz]),
     "purlin_plan_describe": (_i, [_i, _i, _i, _SZP, ctypes.POINTER(ctypes.c_uint64),
                                   ctypes.POINTER(ctypes.c_uint64), _i, ctypes.POINTER(purlin_tune),
                                   ctypes.POINTER(purlin_item), _sz, _SZP, ctypes.POINTER(_i),
@@ -264,6 +265,22 @@ def purlin_set_wait_timeout_ns(h, ns: int) -> int:
 
 def purlin_debug_drop_notify(h, item: int) -> int:
     return load().purlin_debug_drop_notify(h, item)
+
+
+def purlin_trace_enable(h, buffer=None, buffer_bytes: int = 0) -> int:
+    return load().purlin_trace_enable(h, _addr(buffer) or None, buffer_bytes)
+
+
+def trace_records(raw_bytes):
+    """Decode a trace buffer (bytes or uint8 array): (count, list of record dicts)."""
+    import numpy as np
+    b = np.frombuffer(bytes(raw_bytes), dtype=np.uint8)
+    count = int(b[:8].view(np.uint64)[0])
+    rec = np.dtype([("start_ns", "<u8"), ("end_ns", "<u8"), ("cta", "<u4"), ("item", "<u4"),
+                    ("wait_ns", "<u4"), ("len_kib", "<u4")])
+    cap = (b.size - 8) // 32
+    arr = b[8:8 + 32 * cap].view(rec)[:min(count, cap)]
+    return count, [{k: int(r[k]) for k in rec.names} for r in arr]
 
 
 def purlin_query(h):

@@ -237,6 +237,16 @@ purlin_status purlin_set_wait_timeout_ns(purlin_handle h, uint64_t ns);
  * the device status reads PL_ERR_TIMEOUT.  -1 clears. */
 purlin_status purlin_debug_drop_notify(purlin_handle h, long long item);
 
+/* Trace every work item of later calls on the handle into `buffer`, device
+ * memory owned by the caller, 8-byte aligned, `buffer_bytes` long (Iris docs,
+ * "Device Context": device-side event tracing of a collective).  Layout: one
+ * 64-bit count of records, then 32-byte records {u64 start_ns, u64 end_ns,
+ * u32 cta, u32 item, u32 wait_ns, u32 length_KiB} in completion order, times
+ * from %globaltimer.  The caller zeroes the count before the calls it wants
+ * traced; records beyond the buffer's capacity are counted, not written.
+ * NULL stops tracing. */
+purlin_status purlin_trace_enable(purlin_handle h, void* buffer, size_t buffer_bytes);
+
 /* Device facts the handle uses: SM count, compute capability (major*10+minor),
  * and the largest number of CTAs of the reduce kernel resident per SM. */
 purlin_status purlin_query(purlin_handle h, int* sm_count, int* arch, int* max_ctas_per_sm);

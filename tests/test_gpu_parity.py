@@ -617,3 +617,34 @@ def test_bulk_shifted_copies(smis, dmis):
         want = oracle.all_gather(ins)
         for r in range(world):
             assert np.array_equal(outs[r], want[r]), (S, r)
+
+
+@pytest.mark.parametrize("path", [P.PATH_REGISTER, P.PATH_BULK])
+def test_trace_records_every_item(path):
+    world, n = 4, 1 << 18
+    ins = [draw("f32", n) for _ in range(world)]
+    src = RankBuffers([n * 4] * world)
+    dst = RankBuffers([n * 4] * world)
+    src.upload(ins)
+    tune = {"layout": P.PL_LAYOUT_TWO_SHOT, "chunk_bytes": 16384, "path": path, "stages": 2}
+    st, items, grid, _ = P.purlin_plan_describe(P.PL_COLL_ALL_REDUCE, world, P.PL_F32, [n * 4],
+                                                src.ptrs(), dst.ptrs(), 152, tune)
+    assert st == P.PL_OK
+    cap = len(items) + 16
+    buf = torch.zeros(8 + 32 * cap, dtype=torch.uint8, device="cuda:0")
+    h = Handle(world)
+    P.check(P.purlin_tune_override(h.h, tune))
+    P.check(P.purlin_trace_enable(h.h, buf, buf.numel()))
+    P.check(P.purlin_all_reduce(h.h, src.ptrs(), dst.ptrs(), n * 4, P.PL_F32, 0, stream()))
+    sync()
+    P.check(P.purlin_trace_enable(h.h, None, 0))
+    assert h.close() == P.PL_OK
+    count, recs = P.trace_records(buf.cpu().numpy().tobytes())
+    assert count == len(items)
+    assert sorted(r["item"] for r in recs) == list(range(len(items)))
+    for r in recs:
+        assert r["end_ns"] >= r["start_ns"]
+        assert r["cta"] == r["item"] % grid      # two-shot plans deal items round-robin
+    want = oracle.all_reduce(ins, "f32")
+    for r in range(world):
+        assert np.array_equal(bits(dst.read(r, np.float32)), bits(want[r]))

@@ -182,9 +182,13 @@ def test_full_size_plans_are_balanced():
     ]:
         items, grid, _ = _describe(coll, world, dtype, sizes)
         per = np.zeros(grid, np.int64)
+        nitems = np.zeros(grid, np.int64)
         for it in items:
             per[it["cta"]] += it["len"]
-        assert per.max() - per.min() <= 1024, (coll, per.min(), per.max())
+            nitems[it["cta"]] += 1
+        # each part is the exact share rounded to 512 bytes
+        assert per.max() - per.min() <= 1024 * nitems.max(), (coll, per.min(), per.max())
+        assert per.max() <= 1.01 * per.mean()
         for it in items:   # every CTA share starts on a 512-byte boundary of its piece
             assert it["src_off"] % 512 == 0 and it["dst_off"] % 512 == 0
 
@@ -200,8 +204,14 @@ def test_interleaved_plans(interleave):
         ins = [_draw(dtype, n) for _ in range(world)]
         items, grid, nflags = _describe(P.PL_COLL_ALL_REDUCE, world, DT[dtype], [n * E], sm=7, tune=tune)
         assert nflags == 0
-        for i, it in enumerate(items):
-            assert it["cta"] == i % grid and it["len"] <= interleave
+        # CTA c runs parts c, c + grid, ...: its items are not contiguous in the buffer
+        # unless there is one part per CTA, and consecutive items of a CTA are grid parts apart
+        per = {}
+        for it in items:
+            per.setdefault(it["cta"], []).append(it)
+        for c, its in per.items():
+            offs = [it["dst_off"] for it in sorted(its, key=lambda t: t["order"])]
+            assert offs == sorted(offs)
         outs = [np.zeros(n * E, np.uint8) for _ in range(world)]
         run_items(items, [_bytes(x) for x in ins], outs, dtype)
         want = oracle.all_reduce(ins, dtype)
