@@ -212,26 +212,25 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-def source_hash():
+def source_hash(files):
+    """Hash of the given repository files (the sources a kernel is built from)."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "collective_datapath_reduce_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for rel in sorted(files):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(rel.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(name):
     """DRAM bytes per launch of the workload's kernel from the committed ncu summary,
-    or None when the kernel sources changed since the counters were taken."""
+    or None when a source of that kernel changed since the counters were taken."""
     p = os.path.join(ROOT, "profiles", f"{name}.traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
-    except (OSError, ValueError):
-        return None
-    if d.get("src_hash") != source_hash():
+        if d.get("src_hash") != source_hash(d["files"]):
+            return None
+    except (OSError, ValueError, KeyError):
         return None
     return d.get("dram_bytes_per_launch")
 

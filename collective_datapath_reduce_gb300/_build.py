@@ -42,7 +42,7 @@ def _sources():
 
 def _headers():
     return sorted(glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh"))
-                  + glob.glob(os.path.join(INCLUDE, "*.h")))
+                  + glob.glob(os.path.join(INCLUDE, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.cuh")))
 
 
 def _newest(paths):

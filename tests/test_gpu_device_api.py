@@ -1,0 +1,125 @@
+"""Device-side collectives (include/purlin_device.cuh) fused into a user kernel.
+
+tests/device_api/fused.cu writes the ranks' sources inside the kernel, calls
+the collective, then reads the destinations; it is compiled here with nvcc
+against the public headers only.  Outputs must equal the oracle bit for bit,
+and the post-call reads must see every CTA's results.
+"""
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from collective_datapath_reduce_gb300 import _build, inputs
+
+pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "device_api", "fused.cu")
+OUT = os.path.join(HERE, "device_api", "_build", "libfused.so")
+MAXR = 16
+
+
+class Context(ctypes.Structure):
+    _fields_ = [("world", ctypes.c_int), ("src", ctypes.c_void_p * MAXR), ("dst", ctypes.c_void_p * MAXR),
+                ("barrier", ctypes.c_void_p), ("timeout_ns", ctypes.c_ulonglong)]
+
+
+class FusedArgs(ctypes.Structure):
+    _fields_ = [("ctx", Context), ("inp", ctypes.c_void_p * MAXR), ("post", ctypes.c_void_p * MAXR),
+                ("bytes", ctypes.c_ulonglong), ("out_bytes", ctypes.c_ulonglong), ("which", ctypes.c_int),
+                ("coll_blocks", ctypes.c_int), ("status", ctypes.c_void_p)]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    os.makedirs(os.path.dirname(OUT), exist_ok=True)
+    if not os.path.exists(OUT) or os.path.getmtime(OUT) < max(
+            os.path.getmtime(SRC), os.path.getmtime(os.path.join(_build.INCLUDE, "purlin_device.cuh")),
+            os.path.getmtime(os.path.join(_build.INCLUDE, "purlin_atoms.cuh"))):
+        cmd = [_build.nvcc(), *_build.ARCH, *_build.CFLAGS, "-shared", SRC, "-o", OUT]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        assert r.returncode == 0, r.stdout + r.stderr
+    L = ctypes.CDLL(OUT)
+    assert L.fused_args_bytes() == ctypes.sizeof(FusedArgs)
+    return L
+
+
+def run(L, which, world, ins, out_bytes, coll_frac=1.0):
+    dev = torch.device("cuda", 0)
+    nbytes = ins[0].nbytes
+    tin = [torch.from_numpy(np.ascontiguousarray(a).view(np.uint8).copy()).to(dev) for a in ins]
+    src = [torch.zeros(nbytes, dtype=torch.uint8, device=dev) for _ in range(world)]
+    dst = [torch.zeros(out_bytes, dtype=torch.uint8, device=dev) for _ in range(world)]
+    post = [torch.zeros(out_bytes, dtype=torch.uint8, device=dev) for _ in range(world)]
+    bar = torch.zeros(2, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    grid = ctypes.c_int()
+    assert L.fused_max_grid(ctypes.byref(grid)) == 0
+    g = grid.value
+    f = FusedArgs()
+    f.ctx.world = world
+    for r in range(world):
+        f.ctx.src[r] = src[r].data_ptr()
+        f.ctx.dst[r] = dst[r].data_ptr()
+        f.inp[r] = tin[r].data_ptr()
+        f.post[r] = post[r].data_ptr()
+    f.ctx.barrier = bar.data_ptr()
+    f.ctx.timeout_ns = 0
+    f.bytes = nbytes
+    f.out_bytes = out_bytes
+    f.which = which
+    f.coll_blocks = max(1, int(g * coll_frac))
+    f.status = status.data_ptr()
+    for _ in range(2):       # twice: the barrier words are reused across launches
+        rc = L.fused_launch(ctypes.byref(f), g, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert rc == 0, rc
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+    outs = [d.cpu().numpy() for d in dst]
+    for r in range(world):
+        assert np.array_equal(post[r].cpu().numpy(), (outs[r].astype(np.int32) + 1).astype(np.uint8))
+    return outs
+
+
+@pytest.mark.parametrize("coll_frac", [1.0, 0.3])
+def test_fused_all_gather_and_all_to_all(lib, coll_frac):
+    rng = np.random.default_rng(31)
+    world, S = 8, (1 << 20) + 48
+    ins = [rng.integers(0, 256, size=S, dtype=np.uint8) for _ in range(world)]
+    outs = run(lib, 0, world, ins, world * S, coll_frac)
+    want = oracle.all_gather([x ^ 0x5A for x in ins])
+    for r in range(world):
+        assert np.array_equal(outs[r], want[r])
+    world, S = 4, 4 * 100001
+    ins = [rng.integers(0, 256, size=S, dtype=np.uint8) for _ in range(world)]
+    outs = run(lib, 1, world, ins, S, coll_frac)
+    want = oracle.all_to_all([x ^ 0x5A for x in ins])
+    for r in range(world):
+        assert np.array_equal(outs[r], want[r])
+
+
+def test_fused_reductions(lib):
+    rng = np.random.default_rng(32)
+    world, n = 5, 300001
+    ins = [inputs.to_bf16_bits(rng.standard_normal(n).astype(np.float32)) for _ in range(world)]
+    outs = run(lib, 2, world, ins, n * 2)
+    want = oracle.all_reduce(ins, "bf16")
+    for r in range(world):
+        assert np.array_equal(outs[r].view(np.uint16), want[r])
+    world, c = 8, 70001
+    ins = [rng.standard_normal(world * c).astype(np.float32) for _ in range(world)]
+    outs = run(lib, 3, world, ins, c * 4)
+    want = oracle.reduce_scatter(ins, "f32")
+    for r in range(world):
+        assert np.array_equal(outs[r].view(np.uint32), want[r].view(np.uint32))
+    ins = [rng.standard_normal(100003).astype(np.float32) for _ in range(world)]
+    outs = run(lib, 4, world, ins, 100003 * 4, 0.5)
+    want = oracle.all_reduce(ins, "f32")
+    for r in range(world):
+        assert np.array_equal(outs[r].view(np.uint32), want[r].view(np.uint32))
