@@ -219,7 +219,7 @@ static int validate_tune(const Tune& t) {
   if (t.stages < 2 || t.stages > 8) return PL_ERR_INVALID_ARG;
   if (t.store_hint < 1 || t.store_hint > 2) return PL_ERR_INVALID_ARG;
   if (t.min_cta_bytes < 16) return PL_ERR_INVALID_ARG;
-  if (t.interleave_bytes < 0 || (t.interleave_bytes && (t.interleave_bytes < 512 || t.interleave_bytes % 512)))
+  if (t.interleave_bytes < -1 || (t.interleave_bytes > 0 && (t.interleave_bytes < 512 || t.interleave_bytes % 512)))
     return PL_ERR_INVALID_ARG;
   return PL_OK;
 }
@@ -254,6 +254,7 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
   }
   p.tune = tune_merge(tune_table(coll, world, dtype, per_rank), tune_in);
   if (int st = validate_tune(p.tune)) return st;
+  if (p.tune.interleave_bytes < 0) p.tune.interleave_bytes = 0;  // -1 in an override: contiguous shares
   if (max_ctas_per_sm > 0) p.tune.ctas_per_sm = std::min(p.tune.ctas_per_sm, max_ctas_per_sm);
 
   const uint32_t ALL = all_ranks(world);

@@ -104,9 +104,9 @@ typedef struct {
   int stages;       /* TMA pipeline depth, 2..8 */
   int store_hint;   /* 1 = default write-back stores, 2 = streaming (evict-first) stores */
   int min_cta_bytes;/* fewest work bytes given to one CTA before the grid shrinks */
-  int interleave_bytes; /* 0: each CTA takes one contiguous share of the work; a multiple
-                           of 512: the work is cut into tiles of this size dealt
-                           round-robin to the CTAs */
+  int interleave_bytes; /* a multiple of 512: the work is cut into k x grid parts of about
+                           this size and CTA c takes parts c, c + grid, ...; -1: one
+                           contiguous share per CTA (0 = the table's choice) */
 } purlin_tune;
 
 /* One work item of a plan, as purlin_plan_describe reports it. */
