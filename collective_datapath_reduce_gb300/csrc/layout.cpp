@@ -98,11 +98,12 @@ size_t n_sizes(int coll, int world) {
 // Tuning table, from the sweeps measured on a GB300 (152 SMs, HBM3e):
 // `bytes_per_rank` is the per-rank size the collective moves (for the V
 // variants, their total divided by the world).  Summary of what won:
-//   AllReduce   register path, 256 threads x 2 CTAs/SM; from 32 MiB per rank
-//               16 KiB tiles dealt round-robin with evict-first stores (94% of
-//               the measured copy bandwidth at 8 x 64 MiB bf16, against 90%
-//               with one contiguous share per CTA); the fewest bytes per CTA
-//               stay at 512 so small calls spread over many CTAs.
+//   AllReduce   register path, 512 threads; from 8 MiB per rank 128 CTAs with
+//               one contiguous share each and evict-first stores (96% of the
+//               measured copy bandwidth at 8 x 64 MiB bf16, 99.9% at 8 x 256
+//               MiB; one CTA per SM or more gave 90-92%: fewer concurrent DRAM
+//               streams win); the fewest bytes per CTA stay at 512 so small
+//               calls spread over many CTAs.
 //   ReduceScatter  from 8 MiB per rank the TMA bulk ring (2 slots x 32 KiB
 //               per source) runs above the copy bandwidth: the traffic is
 //               8 reads per write.  Below that, the register path.
@@ -129,17 +130,12 @@ Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
     case kAtomReduce:
       t.unroll = world <= 4 ? 2 : 1;
       t.chunk_bytes = 64 * 1024;  // two-shot tile
-      if (S >= 32 * MiB) {
-        // 16 KiB tiles dealt round-robin with evict-first stores: all CTAs
-        // sweep neighbouring addresses of the 2N buffers together
-        t.interleave_bytes = 16 * 1024;
+      t.threads = 512;
+      if (S >= 8 * MiB) {
+        // 128 CTAs of 512 threads, one contiguous share each, evict-first
+        // stores: fewer concurrent DRAM streams than one CTA per SM
+        t.max_ctas = 128;
         t.store_hint = 2;
-      } else if (S >= 8 * MiB) {
-        t.threads = 512;
-        t.interleave_bytes = (int)std::min<uint64_t>(128 * KiB, std::max<uint64_t>(16 * KiB, S / 128));
-        t.store_hint = 2;
-      } else {
-        t.threads = 512;
       }
       break;
     case kReduceScatter:
@@ -206,6 +202,7 @@ Tune tune_merge(const Tune& b, const Tune& o) {
   if (o.store_hint) t.store_hint = o.store_hint;
   if (o.min_cta_bytes) t.min_cta_bytes = o.min_cta_bytes;
   if (o.interleave_bytes) t.interleave_bytes = o.interleave_bytes;
+  if (o.max_ctas) t.max_ctas = o.max_ctas;
   return t;
 }
 
@@ -221,6 +218,7 @@ static int validate_tune(const Tune& t) {
   if (t.min_cta_bytes < 16) return PL_ERR_INVALID_ARG;
   if (t.interleave_bytes < -1 || (t.interleave_bytes > 0 && (t.interleave_bytes < 512 || t.interleave_bytes % 512)))
     return PL_ERR_INVALID_ARG;
+  if (t.max_ctas < 0) return PL_ERR_INVALID_ARG;
   return PL_OK;
 }
 
@@ -432,7 +430,8 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
   if (!p.reduce) p.nsrc = 1;
 
   // ------------------------------------------------------------ tiling
-  const uint64_t gcap = (uint64_t)p.tune.ctas_per_sm * (uint64_t)sm_count;
+  uint64_t gcap = (uint64_t)p.tune.ctas_per_sm * (uint64_t)sm_count;
+  if (p.tune.max_ctas > 0) gcap = std::min<uint64_t>(gcap, (uint64_t)p.tune.max_ctas);
   if (sync) {
     p.strided = true;
     p.sync = true;

@@ -63,7 +63,8 @@ struct Tune {
   int stages = 0;
   int store_hint = 0;
   int min_cta_bytes = 0;
-  int interleave_bytes = 0;  // > 0: tiles of this size dealt round-robin to the CTAs
+  int interleave_bytes = 0;  // > 0: parts of about this size, CTA c takes parts c, c + grid, ...
+  int max_ctas = 0;          // > 0: cap on the grid size
 };
 
 struct Plan {

@@ -107,6 +107,7 @@ typedef struct {
   int interleave_bytes; /* a multiple of 512: the work is cut into k x grid parts of about
                            this size and CTA c takes parts c, c + grid, ...; -1: one
                            contiguous share per CTA (0 = the table's choice) */
+  int max_ctas;     /* > 0: at most this many CTAs (fewer concurrent DRAM streams) */
 } purlin_tune;
 
 /* One work item of a plan, as purlin_plan_describe reports it. */
