@@ -397,76 +397,108 @@ def run_own(args, dist):
         "pct_of_hbm_peak": round(100 * value / dist.world / peak, 2),
     }
     if extras:
-        line["collectives"] = extras
+        line["vs_size"] = extras
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
     dist.close()
 
 
 def side_table(P, h, stream, dev):
-    """A few more points of the metric (GB/s by collective and size) and the
-    device-to-device memcpy ceiling, each a short event-timed loop."""
+    """The metric against size: GB/s (algorithmic bytes) and microseconds per
+    call for every collective over the workloads' size range, the two-shot
+    AllReduce layout, the two Atoms, and the device-to-device copy ceiling of
+    the same traffic.  Each point is one CUDA graph of 10 calls (the pages'
+    graphLaunches knob) replayed after warm-up, timed with events."""
     import torch
     gen = torch.Generator(device=dev)
     gen.manual_seed(7)
-    out = {}
+    GRAPH = 10
+    MI = 1 << 20
 
-    def timeit(fn, iters=20):
-        for _ in range(3):
-            fn()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
-        a.record(stream)
-        for _ in range(iters):
-            fn()
-        b.record(stream)
-        torch.cuda.synchronize(dev)
-        return a.elapsed_time(b) / iters
+    def timeit(fn, reps=3):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(GRAPH):
+                    fn()
+            g.replay()
+            best = None
+            for _ in range(reps):
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+                stream.synchronize()
+                ms = a.elapsed_time(b) / GRAPH
+                best = ms if best is None else min(best, ms)
+            del g
+            return best
 
     def bufs(n, count, dtype=torch.uint8):
         if dtype == torch.uint8:
-            return [torch.randint(0, 256, (n,), dtype=torch.uint8, device=dev, generator=gen) for _ in range(count)]
-        return [torch.randn(n, dtype=dtype, device=dev, generator=gen) for _ in range(count)]
+            return [torch.randint(0, 256, (max(n, 1),), dtype=torch.uint8, device=dev, generator=gen)
+                    for _ in range(count)]
+        return [torch.randn(max(n, 1), dtype=dtype, device=dev, generator=gen) for _ in range(count)]
 
-    def gbps(nbytes, ms):
-        return round(nbytes / (ms / 1e3) / 1e9, 1)
+    def point(nbytes, ms):
+        return {"bytes": nbytes, "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms / 1e3) / 1e9, 1)}
 
-    with torch.cuda.stream(stream):
-        for mib in (64, 256):
-            n = mib << 20
-            a, b = bufs(n, 1)[0], torch.empty(n, dtype=torch.uint8, device=dev)
-            ms = timeit(lambda: b.copy_(a))
-            out[f"d2d_memcpy_{mib}MiB"] = {"GB/s": gbps(2 * n, ms), "us": round(ms * 1e3, 2)}
-            del a, b
-        # ReduceScatter fp32, 8 x 256 MiB -> 8 x 32 MiB
-        n = 64 << 20
-        src = bufs(n, WORLD, torch.float32)
-        dstb = [torch.empty(n // WORLD, dtype=torch.float32, device=dev) for _ in range(WORLD)]
-        ms = timeit(lambda: P.check(P.purlin_reduce_scatter(h, src, dstb, n * 4, P.PL_F32, 0, stream)))
-        out["reduce_scatter_f32_8x256MiB"] = {"GB/s": gbps(WORLD * n * 4 + n * 4, ms), "us": round(ms * 1e3, 1)}
-        del src, dstb
-        # AllReduce two-shot layout at the headline size
-        srcb = bufs(N_ELEMS, WORLD, torch.bfloat16)
-        dstb = [torch.empty_like(t) for t in srcb]
-        P.check(P.purlin_tune_override(h, {"layout": P.PL_LAYOUT_TWO_SHOT}))
-        ms = timeit(lambda: P.check(P.purlin_all_reduce(h, srcb, dstb, S, P.PL_BF16, 0, stream)))
-        out["all_reduce_two_shot_bf16_8x64MiB"] = {"GB/s": gbps(ALGO_BYTES, ms), "us": round(ms * 1e3, 1)}
-        P.check(P.purlin_tune_override(h, None))
-        del srcb, dstb
-        # AllGather / AllToAll u8 at 1 KiB, 1 MiB, 64 MiB per rank
-        for size in (1 << 10, 1 << 20, 64 << 20):
-            src = bufs(size, WORLD)
-            dag = [torch.empty(WORLD * size, dtype=torch.uint8, device=dev) for _ in range(WORLD)]
-            ms = timeit(lambda: P.check(P.purlin_all_gather(h, src, dag, size, stream)))
-            out[f"all_gather_u8_8x{size >> 10}KiB"] = {"GB/s": gbps(WORLD * size * (1 + WORLD), ms),
-                                                       "us": round(ms * 1e3, 2)}
-            del dag
-            da = [torch.empty(size, dtype=torch.uint8, device=dev) for _ in range(WORLD)]
-            ms = timeit(lambda: P.check(P.purlin_all_to_all(h, src, da, size, stream)))
-            out[f"all_to_all_u8_8x{size >> 10}KiB"] = {"GB/s": gbps(2 * WORLD * size, ms), "us": round(ms * 1e3, 2)}
-            del src, da
+    out = {"d2d_copy": {}, "all_gather_u8": {}, "all_to_all_u8": {}, "all_reduce_bf16": {},
+           "reduce_scatter_f32": {}, "all_reduce_two_shot_bf16": {}, "atom_copy": {}, "atom_reduce": {}}
+    chk = lambda st: P.check(st)
+    for size in [1 << (10 + 2 * k) for k in range(10)]:          # 1 KiB .. 256 MiB per rank
+        key = f"{size >> 10}KiB" if size < MI else f"{size >> 20}MiB"
+        src = bufs(size, WORLD)
+        dag = [torch.empty(WORLD * size, dtype=torch.uint8, device=dev) for _ in range(WORLD)]
+        out["all_gather_u8"][key] = point(WORLD * size * (1 + WORLD),
+                                          timeit(lambda: chk(P.purlin_all_gather(h, src, dag, size, stream))))
+        del dag
+        da = [torch.empty(size, dtype=torch.uint8, device=dev) for _ in range(WORLD)]
+        out["all_to_all_u8"][key] = point(2 * WORLD * size,
+                                          timeit(lambda: chk(P.purlin_all_to_all(h, src, da, size, stream))))
+        big = torch.empty(2 * WORLD * size, dtype=torch.uint8, device=dev)
+        half = WORLD * size
+        out["d2d_copy"][key] = point(2 * half, timeit(lambda: big[half:].copy_(big[:half])))
+        del src, da, big
         torch.cuda.empty_cache()
+    for size in (64 << 10, 1 * MI, 16 * MI, 64 * MI, 256 * MI):
+        key = f"{size >> 10}KiB" if size < MI else f"{size >> 20}MiB"
+        x = bufs(size // 2, WORLD, torch.bfloat16)
+        y = [torch.empty_like(t) for t in x]
+        out["all_reduce_bf16"][key] = point(2 * WORLD * size, timeit(
+            lambda: chk(P.purlin_all_reduce(h, x, y, size, P.PL_BF16, 0, stream))))
+        if size >= 16 * MI:
+            P.check(P.purlin_tune_override(h, {"layout": P.PL_LAYOUT_TWO_SHOT}))
+            out["all_reduce_two_shot_bf16"][key] = point(2 * WORLD * size, timeit(
+                lambda: chk(P.purlin_all_reduce(h, x, y, size, P.PL_BF16, 0, stream))))
+            P.check(P.purlin_tune_override(h, None))
+        del x, y
+        x = bufs(size // 4, WORLD, torch.float32)
+        y = [torch.empty(size // 4 // WORLD, dtype=torch.float32, device=dev) for _ in range(WORLD)]
+        out["reduce_scatter_f32"][key] = point(WORLD * size + size, timeit(
+            lambda: chk(P.purlin_reduce_scatter(h, x, y, size, P.PL_F32, 0, stream))))
+        del x, y
+        torch.cuda.empty_cache()
+    for size in (64 * MI, 256 * MI):
+        a = bufs(size, 1)[0]
+        b = torch.empty(size, dtype=torch.uint8, device=dev)
+        out["atom_copy"][f"1to1_{size >> 20}MiB"] = point(2 * size, timeit(
+            lambda: chk(P.purlin_atom_copy(h, a, [b], size, stream))))
+        del a, b
+    size = 64 * MI
+    for dt, code, nm in ((torch.bfloat16, P.PL_BF16, "bf16"), (torch.float32, P.PL_F32, "f32")):
+        x = bufs(size // (2 if nm == "bf16" else 4), WORLD, dt)
+        for nd in (1, WORLD):
+            y = [torch.empty_like(x[0]) for _ in range(nd)]
+            out["atom_reduce"][f"{nm}_8to{nd}_64MiB"] = point((WORLD + nd) * size, timeit(
+                lambda: chk(P.purlin_atom_reduce(h, x, y, size, code, stream))))
+            del y
+        del x
+    torch.cuda.empty_cache()
     return out
 
 
