@@ -221,14 +221,15 @@ def source_hash(files):
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(name):
+def recorded_traffic(name, tune):
     """DRAM bytes per launch of the workload's kernel from the committed ncu summary,
-    or None when a source of that kernel changed since the counters were taken."""
+    or None when the kernel changed since the counters were taken: a source file
+    it is built from, or its launch configuration (the tuning in use)."""
     p = os.path.join(ROOT, "profiles", f"{name}.traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
-        if d.get("src_hash") != source_hash(d["files"]):
+        if d.get("src_hash") != source_hash(d["files"]) or d.get("tune") != tune:
             return None
     except (OSError, ValueError, KeyError):
         return None
@@ -368,7 +369,7 @@ def run_own(args, dist):
     peak, peak_kind = measured_peaks()
     achieved = wl.algo_bytes / (kernel_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(wl.name),
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(wl.name, tune),
                 "peak_source": f"hbm_gbs of {peak_kind}", "kernel_ms": round(kernel_ms, 5),
                 "algorithmic_bytes_per_launch": wl.algo_bytes}
 
