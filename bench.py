@@ -272,15 +272,16 @@ def run_own(args, dist):
         if st != P.PL_OK:
             raise P.PurlinError(st, wl.name)
 
-    for _ in range(args.warmup):
-        step()
-    stream.synchronize()
     _, tune = P.purlin_tune_get(h, wl.coll, {"bf16": P.PL_BF16, "f32": P.PL_F32, "u8": P.PL_U8}[wl.dtype],
                                 wl.tune_bytes)
-
+    # The clock sampler starts first; the warm-up steps then run straight into
+    # the timed region, so the GPU does not sit idle (and clock down) in between.
     clocks = ClockSampler(dist.local)
     clocks.start()
     time.sleep(0.3)
+    for _ in range(args.warmup):
+        step()
+    stream.synchronize()
     K = args.steps
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -407,20 +408,34 @@ def run_own(args, dist):
 def side_table(P, h, stream, dev):
     """The metric against size: GB/s (algorithmic bytes) and microseconds per
     call for every collective over the workloads' size range, the two-shot
-    AllReduce layout, the two Atoms, and the device-to-device copy ceiling of
-    the same traffic.  Each point is one CUDA graph of 10 calls (the pages'
-    graphLaunches knob) replayed after warm-up, timed with events."""
+    AllReduce layout, the two Atoms, and the device-to-device copy of the same
+    traffic.  Each library point is one CUDA graph of 10 calls (the pages'
+    graphLaunches knob) replayed after warm-up, timed with events; the copy
+    reference is 10 plain launches of torch's copy kernel."""
     import torch
     gen = torch.Generator(device=dev)
     gen.manual_seed(7)
     GRAPH = 10
     MI = 1 << 20
 
-    def timeit(fn, reps=3):
+    def timeit(fn, reps=3, graph=True):
         with torch.cuda.stream(stream):
             for _ in range(3):
                 fn()
             stream.synchronize()
+            if not graph:
+                best = None
+                for _ in range(reps):
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    for _ in range(GRAPH):
+                        fn()
+                    b.record(stream)
+                    stream.synchronize()
+                    ms = a.elapsed_time(b) / GRAPH
+                    best = ms if best is None else min(best, ms)
+                return best
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for _ in range(GRAPH):
@@ -463,7 +478,9 @@ def side_table(P, h, stream, dev):
                                           timeit(lambda: chk(P.purlin_all_to_all(h, src, da, size, stream))))
         big = torch.empty(2 * WORLD * size, dtype=torch.uint8, device=dev)
         half = WORLD * size
-        out["d2d_copy"][key] = point(2 * half, timeit(lambda: big[half:].copy_(big[:half])))
+        # the copy kernel torch launches outside a graph (inside one, copy_ becomes
+        # a copy-engine memcpy node, which is slower than an SM copy)
+        out["d2d_copy"][key] = point(2 * half, timeit(lambda: big[half:].copy_(big[:half]), graph=False))
         del src, da, big
         torch.cuda.empty_cache()
     for size in (64 << 10, 1 * MI, 16 * MI, 64 * MI, 256 * MI):
