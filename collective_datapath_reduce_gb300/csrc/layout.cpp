@@ -260,7 +260,10 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
     for (size_t i = 0; i < nsizes; ++i) total += sizes[i];
     per_rank = total / (uint64_t)world;
   }
-  p.tune = tune_merge(tune_table(coll, world, dtype, per_rank), tune_in);
+  // A reduce Atom with one destination moves ReduceScatter-shaped traffic
+  // (N reads per write); with several it is AllReduce-shaped.
+  const int table_coll = (coll == kAtomReduce && nsizes == 3 && sizes[2] == 1) ? (int)kReduceScatter : coll;
+  p.tune = tune_merge(tune_table(table_coll, world, dtype, per_rank), tune_in);
   if (int st = validate_tune(p.tune)) return st;
   if (p.tune.interleave_bytes < 0) p.tune.interleave_bytes = 0;  // -1 in an override: contiguous shares
   if (max_ctas_per_sm > 0) p.tune.ctas_per_sm = std::min(p.tune.ctas_per_sm, max_ctas_per_sm);
