@@ -192,7 +192,7 @@ Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
         } else if (S >= 128 * KiB) {
           t.min_cta_bytes = 8 * 1024;
         } else {
-          t.min_cta_bytes = 2 * 1024;
+          t.min_cta_bytes = 128;  // tiny chunks: one piece per CTA
         }
       }
       break;
@@ -264,6 +264,14 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
   // (N reads per write); with several it is AllReduce-shaped.
   const int table_coll = (coll == kAtomReduce && nsizes == 3 && sizes[2] == 1) ? (int)kReduceScatter : coll;
   p.tune = tune_merge(tune_table(table_coll, world, dtype, per_rank), tune_in);
+  if (coll == kAllReduce && p.tune.layout == kTwoShot) {
+    // the two-shot layout's own best (512 threads, two CTAs per SM, write-back
+    // stores, no grid cap) unless the caller set these fields
+    if (!tune_in.threads) p.tune.threads = 512;
+    if (!tune_in.ctas_per_sm) p.tune.ctas_per_sm = 2;
+    if (!tune_in.store_hint) p.tune.store_hint = 1;
+    if (!tune_in.max_ctas) p.tune.max_ctas = 0;
+  }
   if (int st = validate_tune(p.tune)) return st;
   if (p.tune.interleave_bytes < 0) p.tune.interleave_bytes = 0;  // -1 in an override: contiguous shares
   if (max_ctas_per_sm > 0) p.tune.ctas_per_sm = std::min(p.tune.ctas_per_sm, max_ctas_per_sm);
@@ -464,7 +472,9 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
     uint64_t W = 0;
     for (const Piece& q : pieces) W += q.len;
     uint64_t G = std::max<uint64_t>(1, std::min<uint64_t>(gcap, ceil_div(W, (uint64_t)p.tune.min_cta_bytes)));
-    G = std::min<uint64_t>(G, std::max<uint64_t>(1, W / kSplitGranule));
+    // shares of at least one 512-byte granule, except that pieces smaller than
+    // that may each get a CTA of their own (latency of small calls)
+    G = std::min<uint64_t>(G, std::max<uint64_t>({1, W / kSplitGranule, (uint64_t)pieces.size()}));
     uint64_t k = 1;
     if (p.tune.interleave_bytes > 0) {
       const uint64_t T = (uint64_t)p.tune.interleave_bytes;
