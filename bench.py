@@ -464,7 +464,8 @@ def side_table(P, h, stream, dev):
         return {"bytes": nbytes, "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms / 1e3) / 1e9, 1)}
 
     out = {"d2d_copy": {}, "all_gather_u8": {}, "all_to_all_u8": {}, "all_reduce_bf16": {},
-           "reduce_scatter_f32": {}, "all_reduce_two_shot_bf16": {}, "atom_copy": {}, "atom_reduce": {}}
+           "reduce_scatter_f32": {}, "all_reduce_two_shot_bf16": {}, "reduce_scatter_v_bf16": {},
+           "device_api_fused": {}, "atom_copy": {}, "atom_reduce": {}}
     chk = lambda st: P.check(st)
     for size in [1 << (10 + 2 * k) for k in range(10)]:          # 1 KiB .. 256 MiB per rank
         key = f"{size >> 10}KiB" if size < MI else f"{size >> 20}MiB"
@@ -501,6 +502,42 @@ def side_table(P, h, stream, dev):
             lambda: chk(P.purlin_reduce_scatter(h, x, y, size, P.PL_F32, 0, stream))))
         del x, y
         torch.cuda.empty_cache()
+    # ReduceScatterV: uneven chunks (workload 5's first row of counts), bf16
+    from collective_datapath_reduce_gb300 import inputs as _inputs
+    C5, _ = _inputs.w5_counts(WORLD)
+    counts = [int(v) * 2 for v in C5[0]]
+    total = sum(counts)
+    x = bufs(total // 2, WORLD, torch.bfloat16)
+    y = [torch.empty(max(c, 2) // 2, dtype=torch.bfloat16, device=dev) for c in counts]
+    out["reduce_scatter_v_bf16"][f"{total >> 20}MiB"] = point(WORLD * total + total, timeit(
+        lambda: chk(P.purlin_reduce_scatter_v(h, x, y, counts, P.PL_BF16, 0, stream))))
+    del x, y
+    # Device-side API: the example kernel calling purlin::all_gather /
+    # all_reduce with no work of its own, one cooperative launch per call
+    from collective_datapath_reduce_gb300 import examples as EX
+    size = 64 * MI
+    for which, nm, nb_in, nb_out, alg in ((EX.AG, "all_gather_u8_8x64MiB", size, WORLD * size, 9 * WORLD * size),
+                                          (EX.AR_BF16, "all_reduce_bf16_8x64MiB", size, size, 2 * WORLD * size)):
+        src = bufs(nb_in, WORLD)
+        dst = [torch.empty(nb_out, dtype=torch.uint8, device=dev) for _ in range(WORLD)]
+        bar = torch.zeros(2, dtype=torch.int32, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        f = EX.FusedArgs()
+        f.ctx.world = WORLD
+        for r in range(WORLD):
+            f.ctx.src[r] = src[r].data_ptr()
+            f.ctx.dst[r] = dst[r].data_ptr()
+        f.ctx.barrier = bar.data_ptr()
+        f.bytes, f.out_bytes, f.which, f.work = nb_in, nb_out, which, 0
+        g = EX.max_grid()
+        f.coll_blocks = g
+        f.status = status.data_ptr()
+        ms = timeit(lambda: EX.launch(f, g, stream.cuda_stream), graph=False)
+        if int(status.item()) != 0:
+            raise RuntimeError("device-side collective reported a time-out")
+        out["device_api_fused"][nm] = point(alg, ms)
+        del src, dst
+    torch.cuda.empty_cache()
     for size in (64 * MI, 256 * MI):
         a = bufs(size, 1)[0]
         b = torch.empty(size, dtype=torch.uint8, device=dev)

@@ -22,6 +22,8 @@ BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIBNAME = "libpurlin_gb.so"
 LIBPATH = os.path.join(LIBDIR, LIBNAME)
+EXAMPLES = os.path.join(PKG, "examples")
+EXAMPLES_PATH = os.path.join(LIBDIR, "libpurlin_examples.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # IEEE binary32 arithmetic throughout: no flush-to-zero, no contraction, exact division.
@@ -49,8 +51,32 @@ def _newest(paths):
     return max((os.path.getmtime(p) for p in paths), default=0.0)
 
 
+def build_examples(verbose: bool = False, force: bool = False) -> str:
+    """Compile (if needed) the device-side API examples into libpurlin_examples.so.
+
+    They use only the public headers (include/purlin_device.cuh and
+    include/purlin_atoms.cuh), as a user's own kernels would."""
+    os.makedirs(LIBDIR, exist_ok=True)
+    srcs = sorted(glob.glob(os.path.join(EXAMPLES, "*.cu")))
+    newest = max(_newest(srcs), _newest(glob.glob(os.path.join(INCLUDE, "*.cuh"))))
+    if not force and os.path.exists(EXAMPLES_PATH) and os.path.getmtime(EXAMPLES_PATH) >= newest:
+        return EXAMPLES_PATH
+    tmp = EXAMPLES_PATH + ".tmp"
+    cmd = [nvcc(), *ARCH, "-O3", "-std=c++17", "-lineinfo", "-ftz=false", "-prec-div=true", "-prec-sqrt=true",
+           "-fmad=false", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-shared", *srcs, "-o", tmp]
+    if verbose:
+        cmd.insert(1, "-Xptxas=-v")
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if verbose and (r.stdout or r.stderr):
+        print(r.stdout + r.stderr)
+    if r.returncode != 0:
+        raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
+    os.replace(tmp, EXAMPLES_PATH)
+    return EXAMPLES_PATH
+
+
 def build(verbose: bool = False, force: bool = False) -> str:
-    """Compile (if needed) and return the path of libpurlin_gb.so."""
+    """Compile (if needed) and return the path of libpurlin_gb.so (and the examples library)."""
     os.makedirs(BUILD, exist_ok=True)
     os.makedirs(LIBDIR, exist_ok=True)
     srcs = _sources()
@@ -85,6 +111,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
         if r.returncode != 0:
             raise RuntimeError("link failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
         os.replace(tmp, LIBPATH)
+    build_examples(verbose, force)
     return LIBPATH
 
 

@@ -257,6 +257,12 @@ purlin_status run(purlin_ctx* h, int coll, int world, int dtype, const uint64_t*
   uint8_t sres[pl::kMaxWorld] = {}, dres[pl::kMaxWorld] = {};
   for (int r = 0; r < nin; ++r) sres[r] = (uint8_t)((uintptr_t)in[r] & 15u);
   for (int r = 0; r < nout; ++r) dres[r] = (uint8_t)((uintptr_t)out[r] & 15u);
+  // The workspace and the plans live on the device that was current when the
+  // handle was created; launching with another device current would hand the
+  // kernel pointers of a different GPU.
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return cuda_fail(cudaErrorInvalidDevice);
+  if (cur != h->device) return PL_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(h->mu);
   DevPlan* d = nullptr;
   purlin_status st = get_plan(h, coll, world, dtype, sizes, n, sres, dres, stream, &d);

@@ -191,6 +191,8 @@ Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
           t.min_cta_bytes = 32 * 1024;
         } else if (S >= 128 * KiB) {
           t.min_cta_bytes = 8 * 1024;
+        } else if (S >= 32 * KiB) {
+          t.min_cta_bytes = 2 * 1024;
         } else {
           t.min_cta_bytes = 128;  // tiny chunks: one piece per CTA
         }

@@ -44,6 +44,11 @@ def _check(status, what):
         raise P.PurlinError(status, what)
 
 
+def _on(handle):
+    """Make the handle's device current for the call (the C ABI requires it)."""
+    return torch.cuda.device(handle.device)
+
+
 def _same(tensors, world, what):
     if len(tensors) != world:
         raise ValueError(f"{what}: expected {world} tensors (one per rank), got {len(tensors)}")
@@ -74,8 +79,9 @@ def all_reduce(xs, outs, handle: Handle, stream=None, reduction_mode=ReductionMo
     dt = _DTYPES.get(xs[0].dtype)
     if dt is None or any(t.dtype != xs[0].dtype or t.numel() != xs[0].numel() for t in list(xs) + list(outs)):
         raise ValueError("all_reduce: float32 or bfloat16 tensors of one size")
-    _check(P.purlin_all_reduce(handle.raw, xs, outs, xs[0].numel() * xs[0].element_size(), dt, int(reduction_mode),
-                               _stream(stream, handle.device)), "all_reduce")
+    with _on(handle):
+        _check(P.purlin_all_reduce(handle.raw, xs, outs, xs[0].numel() * xs[0].element_size(), dt, int(reduction_mode),
+                                   _stream(stream, handle.device)), "all_reduce")
 
 
 def reduce_scatter(xs, outs, handle: Handle, stream=None, reduction_mode=ReductionMode.DETERMINISTIC):
@@ -85,31 +91,35 @@ def reduce_scatter(xs, outs, handle: Handle, stream=None, reduction_mode=Reducti
     dt = _DTYPES.get(xs[0].dtype)
     if dt is None:
         raise ValueError("reduce_scatter: float32 or bfloat16 tensors")
-    _check(P.purlin_reduce_scatter(handle.raw, xs, outs, xs[0].numel() * xs[0].element_size(), dt,
-                                   int(reduction_mode), _stream(stream, handle.device)), "reduce_scatter")
+    with _on(handle):
+        _check(P.purlin_reduce_scatter(handle.raw, xs, outs, xs[0].numel() * xs[0].element_size(), dt,
+                                       int(reduction_mode), _stream(stream, handle.device)), "reduce_scatter")
 
 
 def all_gather(xs, outs, handle: Handle, stream=None):
     """outs[r] = concatenation of xs along dim 0, for every rank r."""
     _same(xs, handle.world, "all_gather")
     _same(outs, handle.world, "all_gather")
-    _check(P.purlin_all_gather(handle.raw, xs, outs, xs[0].numel() * xs[0].element_size(),
-                               _stream(stream, handle.device)), "all_gather")
+    with _on(handle):
+        _check(P.purlin_all_gather(handle.raw, xs, outs, xs[0].numel() * xs[0].element_size(),
+                                   _stream(stream, handle.device)), "all_gather")
 
 
 def all_to_all(xs, outs, handle: Handle, stream=None):
     """outs[d] chunk s = xs[s] chunk d (world equal chunks along dim 0)."""
     _same(xs, handle.world, "all_to_all")
     _same(outs, handle.world, "all_to_all")
-    _check(P.purlin_all_to_all(handle.raw, xs, outs, xs[0].numel() * xs[0].element_size(),
-                               _stream(stream, handle.device)), "all_to_all")
+    with _on(handle):
+        _check(P.purlin_all_to_all(handle.raw, xs, outs, xs[0].numel() * xs[0].element_size(),
+                                   _stream(stream, handle.device)), "all_to_all")
 
 
 def all_gather_v(xs, outs, handle: Handle, stream=None):
     """outs[r] = concatenation of all of xs (each rank's tensor in full), packed in rank order."""
     _same(xs, handle.world, "all_gather_v")
-    _check(P.purlin_all_gather_v(handle.raw, xs, outs, [t.numel() * t.element_size() for t in xs],
-                                 _stream(stream, handle.device)), "all_gather_v")
+    with _on(handle):
+        _check(P.purlin_all_gather_v(handle.raw, xs, outs, [t.numel() * t.element_size() for t in xs],
+                                     _stream(stream, handle.device)), "all_gather_v")
 
 
 def all_to_all_v(xs, outs, counts, handle: Handle, stream=None):
@@ -117,7 +127,8 @@ def all_to_all_v(xs, outs, counts, handle: Handle, stream=None):
     _same(xs, handle.world, "all_to_all_v")
     es = xs[0].element_size()
     flat = [int(c) * es for row in counts for c in row]
-    _check(P.purlin_all_to_all_v(handle.raw, xs, outs, flat, _stream(stream, handle.device)), "all_to_all_v")
+    with _on(handle):
+        _check(P.purlin_all_to_all_v(handle.raw, xs, outs, flat, _stream(stream, handle.device)), "all_to_all_v")
 
 
 def reduce_scatter_v(xs, outs, counts, handle: Handle, stream=None, reduction_mode=ReductionMode.DETERMINISTIC):
@@ -127,5 +138,6 @@ def reduce_scatter_v(xs, outs, counts, handle: Handle, stream=None, reduction_mo
     if dt is None:
         raise ValueError("reduce_scatter_v: float32 or bfloat16 tensors")
     es = xs[0].element_size()
-    _check(P.purlin_reduce_scatter_v(handle.raw, xs, outs, [int(c) * es for c in counts], dt, int(reduction_mode),
-                                     _stream(stream, handle.device)), "reduce_scatter_v")
+    with _on(handle):
+        _check(P.purlin_reduce_scatter_v(handle.raw, xs, outs, [int(c) * es for c in counts], dt, int(reduction_mode),
+                                         _stream(stream, handle.device)), "reduce_scatter_v")

@@ -32,7 +32,9 @@
  *   - Reductions need every pointer aligned to the element size; copies take
  *     any byte alignment.  16-byte alignment of every address is the fast path.
  *   - Calls on one handle must be ordered (one stream, or streams the caller
- *     orders): they share the handle's workspace.
+ *     orders): they share the handle's workspace.  They must be made with the
+ *     handle's device current (the one current at purlin_initialize); other
+ *     calls return PL_ERR_INVALID_ARG.
  *   - The first call of a given shape builds its plan (a small host
  *     computation plus one upload); make it before capturing the stream into
  *     a CUDA graph.

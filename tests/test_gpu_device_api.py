@@ -1,53 +1,25 @@
 """Device-side collectives (include/purlin_device.cuh) fused into a user kernel.
 
-tests/device_api/fused.cu writes the ranks' sources inside the kernel, calls
-the collective, then reads the destinations; it is compiled here with nvcc
-against the public headers only.  Outputs must equal the oracle bit for bit,
-and the post-call reads must see every CTA's results.
+The example kernel (collective_datapath_reduce_gb300/examples/
+fused_collectives.cu, built with the public headers only) writes the ranks'
+sources inside the kernel, calls the collective, then reads the destinations.
+Outputs must equal the oracle bit for bit, and the post-call reads must see
+every CTA's results.
 """
-
-import ctypes
-import os
-import subprocess
 
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from collective_datapath_reduce_gb300 import _build, inputs
+from collective_datapath_reduce_gb300 import examples as EX
+from collective_datapath_reduce_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
 
-HERE = os.path.dirname(os.path.abspath(__file__))
-SRC = os.path.join(HERE, "device_api", "fused.cu")
-OUT = os.path.join(HERE, "device_api", "_build", "libfused.so")
-MAXR = 16
-
-
-class Context(ctypes.Structure):
-    _fields_ = [("world", ctypes.c_int), ("src", ctypes.c_void_p * MAXR), ("dst", ctypes.c_void_p * MAXR),
-                ("barrier", ctypes.c_void_p), ("timeout_ns", ctypes.c_ulonglong)]
-
-
-class FusedArgs(ctypes.Structure):
-    _fields_ = [("ctx", Context), ("inp", ctypes.c_void_p * MAXR), ("post", ctypes.c_void_p * MAXR),
-                ("bytes", ctypes.c_ulonglong), ("out_bytes", ctypes.c_ulonglong), ("which", ctypes.c_int),
-                ("coll_blocks", ctypes.c_int), ("status", ctypes.c_void_p)]
-
-
 @pytest.fixture(scope="module")
 def lib():
-    os.makedirs(os.path.dirname(OUT), exist_ok=True)
-    if not os.path.exists(OUT) or os.path.getmtime(OUT) < max(
-            os.path.getmtime(SRC), os.path.getmtime(os.path.join(_build.INCLUDE, "purlin_device.cuh")),
-            os.path.getmtime(os.path.join(_build.INCLUDE, "purlin_atoms.cuh"))):
-        cmd = [_build.nvcc(), *_build.ARCH, *_build.CFLAGS, "-shared", SRC, "-o", OUT]
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        assert r.returncode == 0, r.stdout + r.stderr
-    L = ctypes.CDLL(OUT)
-    assert L.fused_args_bytes() == ctypes.sizeof(FusedArgs)
-    return L
+    return EX.load()
 
 
 def run(L, which, world, ins, out_bytes, coll_frac=1.0):
@@ -59,10 +31,8 @@ def run(L, which, world, ins, out_bytes, coll_frac=1.0):
     post = [torch.zeros(out_bytes, dtype=torch.uint8, device=dev) for _ in range(world)]
     bar = torch.zeros(2, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    grid = ctypes.c_int()
-    assert L.fused_max_grid(ctypes.byref(grid)) == 0
-    g = grid.value
-    f = FusedArgs()
+    g = EX.max_grid()
+    f = EX.FusedArgs()
     f.ctx.world = world
     for r in range(world):
         f.ctx.src[r] = src[r].data_ptr()
@@ -76,8 +46,9 @@ def run(L, which, world, ins, out_bytes, coll_frac=1.0):
     f.which = which
     f.coll_blocks = max(1, int(g * coll_frac))
     f.status = status.data_ptr()
+    f.work = EX.WORK_BEFORE | EX.WORK_AFTER
     for _ in range(2):       # twice: the barrier words are reused across launches
-        rc = L.fused_launch(ctypes.byref(f), g, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        rc = EX.launch(f, g, torch.cuda.current_stream().cuda_stream)
         assert rc == 0, rc
         torch.cuda.synchronize()
         assert int(status.item()) == 0
