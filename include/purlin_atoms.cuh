@@ -14,7 +14,8 @@
 //   pl::reduce_atom<T, NS, U, STREAMING>(src[], ns, dst[], nd, len)
 //       dst[j][i] = fold over s < ns of src[s][i]: binary32 adds in ascending
 //       source order from src[0]'s value, one rounding to T (float or
-//       pl::bf16_tag); pointers aligned to the element size.  NS = ns when the
+//       pl::bf16_tag); pointers aligned to the element size, every dst[j] with
+//       the same address modulo 16.  NS = ns when the
 //       count is known at compile time (2..8), else 0.  A fifth template
 //       argument COHERENT = true makes the loads L2 loads, for sources written
 //       earlier in the same launch.
@@ -80,6 +81,37 @@ __device__ __forceinline__ void st_vec(void* p, uint4 v) {
     asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                  "r"(v.w)
                  : "memory");
+}
+
+// A 16-byte vector stored as pieces of SW bytes (16, 8, 4 or 2): for
+// destinations aligned only to SW.
+template <bool STREAMING, int SW>
+__device__ __forceinline__ void st_parts(void* p, uint4 v) {
+  if constexpr (SW == 16) {
+    st_vec<STREAMING>(p, v);
+  } else if constexpr (SW == 8) {
+    if (STREAMING) {
+      asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+      asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"((char*)p + 8), "r"(v.z), "r"(v.w) : "memory");
+    } else {
+      asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+      asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"((char*)p + 8), "r"(v.z), "r"(v.w) : "memory");
+    }
+  } else if constexpr (SW == 4) {
+    uint32_t* q = reinterpret_cast<uint32_t*>(p);
+    q[0] = v.x;
+    q[1] = v.y;
+    q[2] = v.z;
+    q[3] = v.w;
+  } else {
+    unsigned short* q = reinterpret_cast<unsigned short*>(p);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      q[2 * i] = (unsigned short)(w[i] & 0xFFFFu);
+      q[2 * i + 1] = (unsigned short)(w[i] >> 16);
+    }
+  }
 }
 
 __device__ __forceinline__ unsigned long long globaltimer() {
@@ -253,7 +285,7 @@ __device__ __forceinline__ void reduce_elem(const char* const* src, int ns, char
 // UU vectors starting at index v (stride `step`) of every source: fold and
 // store.  NS > 0: exactly NS sources, all loads issued before the first add.
 // NS == 0: ns sources (up to 16), loaded in batches of 8.
-template <typename T, int NS, int UU, bool STREAMING, bool COHERENT = false>
+template <typename T, int NS, int UU, bool STREAMING, bool COHERENT = false, int SW = 16>
 __device__ __forceinline__ void reduce_step(const char* const* src, int ns, char* const* dst, int nd,
                                             uint64_t off, uint32_t v, uint32_t step) {
   constexpr int EPV = Elem<T>::kPerVec;
@@ -289,20 +321,19 @@ __device__ __forceinline__ void reduce_step(const char* const* src, int ns, char
 #pragma unroll
   for (int u = 0; u < UU; ++u) {
     const uint4 o = Elem<T>::pack(acc[u]);
-    for (int j = 0; j < nd; ++j)
-      st_vec<STREAMING>(reinterpret_cast<uint4*>(dst[j] + off) + v + u * step, o);
+    for (int j = 0; j < nd; ++j) st_parts<STREAMING, SW>(dst[j] + off + (uint64_t)(v + u * step) * 16, o);
   }
 }
 
-template <typename T, int NS, int U, bool STREAMING, bool COHERENT = false>
+template <typename T, int NS, int U, bool STREAMING, bool COHERENT = false, int SW = 16>
 __device__ __forceinline__ void reduce_vec(const char* const* src, int ns, char* const* dst, int nd,
                                            uint64_t off, uint32_t nv) {
   const uint32_t step = blockDim.x;
   uint32_t v = threadIdx.x;
   for (; v + (U - 1) * step < nv; v += U * step)
-    reduce_step<T, NS, U, STREAMING, COHERENT>(src, ns, dst, nd, off, v, step);
+    reduce_step<T, NS, U, STREAMING, COHERENT, SW>(src, ns, dst, nd, off, v, step);
   if (U > 1)
-    for (; v < nv; v += step) reduce_step<T, NS, 1, STREAMING, COHERENT>(src, ns, dst, nd, off, v, step);
+    for (; v < nv; v += step) reduce_step<T, NS, 1, STREAMING, COHERENT, SW>(src, ns, dst, nd, off, v, step);
 }
 
 template <typename T, int NS, int U, bool STREAMING, bool COHERENT = false>
@@ -311,17 +342,28 @@ __device__ void reduce_atom(const char* const* src, int ns, char* const* dst, in
   const uint32_t tid = threadIdx.x, nt = blockDim.x;
   const uint64_t n = len / E;
   const uint32_t res = (uint32_t)((uintptr_t)src[0] & 15u);
-  bool co = ((uintptr_t)dst[0] & 15u) == res;
+  bool co = true;
   for (int s = 1; s < ns; ++s) co = co && (((uintptr_t)src[s] & 15u) == res);
   if (!co) {
     for (uint64_t k = tid; k < n; k += nt) reduce_elem<T, COHERENT>(src, ns, dst, nd, k);
     return;
   }
+  // Vectors follow the sources' 16-byte alignment; the destinations (one
+  // residue for all of them) get each vector in the widest stores their
+  // alignment allows.
   uint64_t head = ((16u - res) & 15u) / E;
   if (head > n) head = n;
   for (uint64_t k = tid; k < head; k += nt) reduce_elem<T, COHERENT>(src, ns, dst, nd, k);
   const uint32_t nv = (uint32_t)(((n - head) * E) >> 4);
-  reduce_vec<T, NS, U, STREAMING, COHERENT>(src, ns, dst, nd, head * E, nv);
+  const uint32_t rd = (uint32_t)(((uintptr_t)dst[0] + head * E) & 15u);
+  if (rd == 0)
+    reduce_vec<T, NS, U, STREAMING, COHERENT, 16>(src, ns, dst, nd, head * E, nv);
+  else if ((rd & 7u) == 0)
+    reduce_vec<T, NS, U, STREAMING, COHERENT, 8>(src, ns, dst, nd, head * E, nv);
+  else if ((rd & 3u) == 0)
+    reduce_vec<T, NS, U, STREAMING, COHERENT, 4>(src, ns, dst, nd, head * E, nv);
+  else
+    reduce_vec<T, NS, U, STREAMING, COHERENT, 2>(src, ns, dst, nd, head * E, nv);
   for (uint64_t k = head + (uint64_t)nv * (16 / E) + tid; k < n; k += nt)
     reduce_elem<T, COHERENT>(src, ns, dst, nd, k);
 }
