@@ -45,7 +45,9 @@ __global__ void __launch_bounds__(256) fused_kernel(const __grid_constant__ Fuse
   switch (f.which) {
     case 0: st = purlin::all_gather(a, f.ctx); break;
     case 1: st = purlin::all_to_all(a, f.ctx); break;
-    case 2: st = purlin::all_reduce<pl::bf16_tag>(a, f.ctx); break;
+    case 2:  // the source count as a template argument when it is the common 8
+      st = N == 8 ? purlin::all_reduce<pl::bf16_tag, 8>(a, f.ctx) : purlin::all_reduce<pl::bf16_tag>(a, f.ctx);
+      break;
     case 3: st = purlin::reduce_scatter<float>(a, f.ctx); break;
     default: st = purlin::all_reduce<float, 8>(a, f.ctx); break;
   }
