@@ -190,19 +190,24 @@ purlin_status get_plan(purlin_ctx* h, int coll, int world, int dtype, const uint
   if (!d->fn) return PL_ERR_UNSUPPORTED;
   d->threads = d->plan.tune.threads;
   if (d->plan.tune.path == pl::kPathBulk) {
-    // ring of `stages` slots; a reduce slot holds nsrc input tiles and one output tile
-    // (a copy slot holds a 16-byte-aligned source window of chunk + 16 bytes
-    // and an output tile, for sources that are not 16-byte aligned)
-    const int tiles = d->plan.nsrc > 1 ? d->plan.nsrc + 1 : 2;
+    // Ring of `stages` slots.  A reduce slot holds nsrc input tiles and one
+    // output tile.  A copy slot holds one chunk, or, for sources that are not
+    // 16-byte aligned, a source window of chunk + 16 bytes; two output tiles
+    // of one chunk each follow the copy slots (the shifted copy cuts its
+    // destination vectors into them).  A reduce ring is always at least as
+    // large as that copy layout, so a reduce plan's copy items fit too.
+    const bool copy_ring = d->plan.nsrc <= 1;
+    const int tiles = copy_ring ? 1 : d->plan.nsrc + 1;
     const int stages = d->plan.tune.stages;
     int64_t ch = d->plan.tune.chunk_bytes;
-    const int64_t fit = (kMaxDynSmem / stages - 16) / tiles;
+    const int64_t fit = copy_ring ? (kMaxDynSmem - 16 * stages) / (stages + 2) : (kMaxDynSmem / stages - 16) / tiles;
     if (ch > fit) ch = fit;
-    if (ch > (1 << 20) / tiles) ch = (1 << 20) / tiles;  // mbarrier transaction count stays below 2^20
+    const int64_t tx_cap = copy_ring ? (1 << 20) / 2 : (1 << 20) / tiles;
+    if (ch > tx_cap) ch = tx_cap;  // mbarrier transaction count stays below 2^20
     ch &= ~(int64_t)15;
     if (ch < 16) return PL_ERR_INVALID_ARG;
     d->ring_chunk = (uint32_t)ch;
-    d->smem = (int)(stages * (tiles * ch + 16));
+    d->smem = copy_ring ? (int)(stages * (ch + 16) + 2 * ch) : (int)(stages * (tiles * ch + 16));
     // The limit is a property of the kernel function, shared by every plan that
     // launches it: raise it to the largest ring any plan may use, never lower it.
     cudaError_t e = cudaFuncSetAttribute(d->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);

@@ -159,13 +159,18 @@ __device__ void bulk_copy_body(BulkRing& R, char* ring, int stages, uint32_t ch,
 // base + k*ch of round_up(m + len, 16) bytes; the window is loaded with one
 // bulk copy (it only spans granules that hold bytes of the source range),
 // every thread cuts its destination vectors out of it with funnel shifts into
-// the slot's output tile, and the leader bulk-stores the tile.  Slot layout:
-// window of ch + 16 bytes, then the output tile of ch bytes.
+// an output tile, and the leader bulk-stores the tile.
+//
+// Shared memory: `stages` windows of ch + 16 bytes, then two output tiles of
+// ch bytes used in turn.  A window is refilled as soon as the shift has read
+// it, so `stages` loads stay in flight while the stores drain from the tiles;
+// tile k % 2 is rewritten only once the stores of chunk k - 2 have read it.
 __device__ void bulk_copy_shifted_body(BulkRing& R, char* ring, int stages, uint32_t ch, const char* src,
                                        char* const* dst, int nd, uint64_t bytes, unsigned long long limit_ns) {
   const uint32_t m = (uint32_t)((uintptr_t)src & 15u);
   const char* base = src - m;
-  const size_t slot = (size_t)2 * ch + 16;
+  const size_t wslot = (size_t)ch + 16;
+  char* const otiles = ring + (size_t)stages * wslot;
   const uint64_t n = (bytes + ch - 1) / ch;
   const uint32_t g0 = R.chunk;
   const bool leader = threadIdx.x == 0;
@@ -177,7 +182,7 @@ __device__ void bulk_copy_shifted_body(BulkRing& R, char* ring, int stages, uint
     const uint32_t s = (g0 + (uint32_t)k) % (uint32_t)stages;
     const uint32_t win = (m + chunk_len(k) + 15u) & ~15u;
     mbar_expect_tx(&R.full[s], win);
-    bulk_load(ring + s * slot, base + k * ch, win, &R.full[s]);
+    bulk_load(ring + s * wslot, base + k * ch, win, &R.full[s]);
   };
   if (leader) {
     const uint64_t pre = n < (uint64_t)stages ? n : (uint64_t)stages;
@@ -188,20 +193,24 @@ __device__ void bulk_copy_shifted_body(BulkRing& R, char* ring, int stages, uint
     const uint32_t g = g0 + (uint32_t)k;
     const uint32_t s = g % (uint32_t)stages;
     const bool ok = mbar_wait(&R.full[s], (g / (uint32_t)stages) & 1u, limit_ns);
-    if (leader) bulk_wait_read_dyn(stages - 1);
+    // one bulk group per chunk: with at most one pending (chunk k-1), the
+    // group of chunk k-2 has read tile k % 2
+    if (leader) bulk_wait_read<1>();
     if (__syncthreads_or(!ok)) {
       if (leader) R.failed = 1;
       break;
     }
     const uint32_t len = chunk_len(k);
-    const uint4* win = reinterpret_cast<const uint4*>(ring + s * slot);
-    uint4* otile = reinterpret_cast<uint4*>(ring + s * slot + ch + 16);
+    const uint4* win = reinterpret_cast<const uint4*>(ring + s * wslot);
+    uint4* otile = reinterpret_cast<uint4*>(otiles + (size_t)(k & 1) * ch);
+#pragma unroll 4
     for (uint32_t v = threadIdx.x; v < len / 16; v += blockDim.x) otile[v] = window16(win[v], win[v + 1], m);
     fence_async_shared();
     __syncthreads();
     if (leader) {
       for (int j = 0; j < nd; ++j) bulk_store(dst[j] + k * ch, otile, len);
       bulk_commit();
+      // every thread has read window s (barrier above): refill it
       if (k + (uint64_t)stages < n) issue_load(k + (uint64_t)stages);
     }
   }

@@ -104,3 +104,34 @@ def w5_payloads(C: np.ndarray, c: np.ndarray, seed: int = 4):
     a2av = [to_bf16_bits(rng.standard_normal(int(C[s].sum()), dtype=np.float32)) for s in range(world)]
     agv = [to_bf16_bits(rng.standard_normal(int(c[s]), dtype=np.float32)) for s in range(world)]
     return a2av, agv
+
+
+class Tiled:
+    """A rank buffer of `n` elements too large to draw element by element.
+
+    One seeded block of `block` elements (N(0,1) for fp32 / bf16, 0..255 for
+    uint8) is drawn once; element i of the buffer is
+    block[(i + shift + 7 * (i // block)) % block], so every block-sized piece
+    of the buffer is a different rotation of the draw.  `chunks()` yields the
+    buffer piece by piece for upload; `at(idx)` gives the elements at chosen
+    positions, so a test can evaluate the oracle on a sample of any buffer.
+    """
+
+    def __init__(self, n: int, dtype: str, seed: int, shift: int = 0, block: int = 16 * MI):
+        self.n, self.dtype, self.shift, self.block = int(n), dtype, int(shift), int(block)
+        rng = np.random.default_rng(seed)
+        if dtype == "u8":
+            self.base = rng.integers(0, 256, size=self.block, dtype=np.uint8)
+        else:
+            x = rng.standard_normal(self.block, dtype=np.float32)
+            self.base = x if dtype == "f32" else to_bf16_bits(x)
+
+    def at(self, idx: np.ndarray) -> np.ndarray:
+        idx = np.asarray(idx, dtype=np.int64)
+        return self.base[(idx + self.shift + 7 * (idx // self.block)) % self.block]
+
+    def chunks(self):
+        for j, start in enumerate(range(0, self.n, self.block)):
+            m = min(self.block, self.n - start)
+            o = (self.shift + 7 * j) % self.block
+            yield start, np.concatenate((self.base[o:], self.base[:o]))[:m]
