@@ -93,7 +93,7 @@ constexpr int kMaxDynSmem = 227 * 1024 - 1024;
 
 const void* pick_kernel(const pl::Plan& p) {
   if (p.tune.path == pl::kPathBulk) {
-    if (p.nsrc <= 1) return pl::kernel_bulk_copy();
+    if (p.nsrc <= 1) return p.tune.schedule == pl::kSchedItem ? pl::kernel_bulk_copy() : pl::kernel_stream_copy();
     if (p.dtype == pl::kF32) return pl::kernel_bulk_reduce_f32(p.nsrc);
     if (p.dtype == pl::kBF16) return pl::kernel_bulk_reduce_bf16(p.nsrc);
     return nullptr;
@@ -190,6 +190,17 @@ purlin_status get_plan(purlin_ctx* h, int coll, int world, int dtype, const uint
   if (!d->fn) return PL_ERR_UNSUPPORTED;
   d->threads = d->plan.tune.threads;
   if (d->plan.tune.path == pl::kPathBulk) {
+    // dynamic shared memory this kernel can take: the per-block opt-in limit
+    // less its static shared memory (and never more than kMaxDynSmem)
+    int max_dyn = kMaxDynSmem;
+    {
+      cudaFuncAttributes fa;
+      int optin = 0;
+      cudaError_t e = cudaFuncGetAttributes(&fa, d->fn);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device);
+      if (e != cudaSuccess) return cuda_fail(e);
+      max_dyn = std::min(max_dyn, optin - (int)fa.sharedSizeBytes);
+    }
     // Ring of `stages` slots.  A reduce slot holds nsrc input tiles and one
     // output tile.  A copy slot holds one chunk, or, for sources that are not
     // 16-byte aligned, a source window of chunk + 16 bytes; two output tiles
@@ -200,7 +211,7 @@ purlin_status get_plan(purlin_ctx* h, int coll, int world, int dtype, const uint
     const int tiles = copy_ring ? 1 : d->plan.nsrc + 1;
     const int stages = d->plan.tune.stages;
     int64_t ch = d->plan.tune.chunk_bytes;
-    const int64_t fit = copy_ring ? (kMaxDynSmem - 16 * stages) / (stages + 2) : (kMaxDynSmem / stages - 16) / tiles;
+    const int64_t fit = copy_ring ? (max_dyn - 16 * stages) / (stages + 2) : (max_dyn / stages - 16) / tiles;
     if (ch > fit) ch = fit;
     const int64_t tx_cap = copy_ring ? (1 << 20) / 2 : (1 << 20) / tiles;
     if (ch > tx_cap) ch = tx_cap;  // mbarrier transaction count stays below 2^20
@@ -210,7 +221,7 @@ purlin_status get_plan(purlin_ctx* h, int coll, int world, int dtype, const uint
     d->smem = copy_ring ? (int)(stages * (ch + 16) + 2 * ch) : (int)(stages * (tiles * ch + 16));
     // The limit is a property of the kernel function, shared by every plan that
     // launches it: raise it to the largest ring any plan may use, never lower it.
-    cudaError_t e = cudaFuncSetAttribute(d->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+    cudaError_t e = cudaFuncSetAttribute(d->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   if (d->plan.sync) {
@@ -284,6 +295,7 @@ purlin_status run(purlin_ctx* h, int coll, int world, int dtype, const uint64_t*
   a.n_items = (uint32_t)d->plan.items.size();
   a.strided = d->plan.strided ? 1u : 0u;
   a.sync = d->plan.sync ? 1u : 0u;
+  a.queue = d->plan.queue ? 1u : 0u;
   a.flags = h->flags;
   a.ctl = h->ctl;
   a.timeout_ns = h->timeout_ns;
@@ -738,7 +750,10 @@ purlin_status purlin_plan_describe(purlin_coll coll, int world, purlin_dtype dty
       o.dst_mask = it.dst_mask;
       o.wait = it.wait;
       o.notify = it.notify;
-      if (p.strided) {
+      if (p.queue) {
+        o.cta = 0xFFFFFFFFu;  // whichever CTA takes it from the queue
+        o.order = (uint32_t)i;
+      } else if (p.strided) {
         o.cta = (uint32_t)(i % (size_t)p.grid);
         o.order = (uint32_t)(i / (size_t)p.grid);
       } else {

@@ -11,7 +11,7 @@
 namespace pl {
 
 // Control words at the start of the workspace.
-enum : int { kCtlStatus = 0, kCtlEpoch = 1, kCtlDone = 2 };
+enum : int { kCtlStatus = 0, kCtlEpoch = 1, kCtlDone = 2, kCtlQueue = 3, kCtlQueueDone = 4 };
 constexpr int kCtlBytes = 256;   // flags start here
 constexpr int kDevTimeout = 7;   // PL_ERR_TIMEOUT
 
@@ -23,8 +23,9 @@ struct KArgs {
   uint32_t n_items;
   uint32_t strided;           // item i on CTA i % grid (else contiguous ranges)
   uint32_t sync;              // the plan has SNAC flags: epoch, status and done counter in use
+  uint32_t queue;             // items are taken from the shared queue counter (streamed copies)
   uint32_t* flags;
-  uint32_t* ctl;              // status, epoch, done counter
+  uint32_t* ctl;              // status, epoch, done counter, queue counter, queue done counter
   unsigned long long timeout_ns;
   uint32_t drop_notify;       // 1 + item whose notify is skipped, or 0
   int nsrc;                   // sources of each reduce item
@@ -56,5 +57,7 @@ const void* kernel_reduce_bf16(int nsrc, int unroll);
 const void* kernel_bulk_copy();
 const void* kernel_bulk_reduce_f32(int nsrc);
 const void* kernel_bulk_reduce_bf16(int nsrc);
+// Streamed bulk copies (one pipeline across a CTA's items; optional shared queue).
+const void* kernel_stream_copy();
 
 }  // namespace pl

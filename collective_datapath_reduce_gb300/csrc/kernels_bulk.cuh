@@ -109,7 +109,7 @@ struct BulkRing {
 
 // Pure-TMA copy of the aligned body [0, bytes) of one item: src -> every dst.
 // Thread 0 only.  Slots hold `ch` bytes each.
-__device__ void bulk_copy_body(BulkRing& R, char* ring, int stages, uint32_t ch, const char* src,
+__device__ inline void bulk_copy_body(BulkRing& R, char* ring, int stages, uint32_t ch, const char* src,
                                char* const* dst, int nd, uint64_t bytes, unsigned long long limit_ns) {
   const uint64_t n = (bytes + ch - 1) / ch;
   const uint32_t g0 = R.chunk;
@@ -165,7 +165,7 @@ __device__ void bulk_copy_body(BulkRing& R, char* ring, int stages, uint32_t ch,
 // ch bytes used in turn.  A window is refilled as soon as the shift has read
 // it, so `stages` loads stay in flight while the stores drain from the tiles;
 // tile k % 2 is rewritten only once the stores of chunk k - 2 have read it.
-__device__ void bulk_copy_shifted_body(BulkRing& R, char* ring, int stages, uint32_t ch, const char* src,
+__device__ inline void bulk_copy_shifted_body(BulkRing& R, char* ring, int stages, uint32_t ch, const char* src,
                                        char* const* dst, int nd, uint64_t bytes, unsigned long long limit_ns) {
   const uint32_t m = (uint32_t)((uintptr_t)src & 15u);
   const char* base = src - m;

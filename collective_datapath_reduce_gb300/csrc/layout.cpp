@@ -41,6 +41,8 @@ struct Piece {
 };
 
 constexpr uint64_t kMaxItemBytes = 1ull << 30;
+// Queue schedule without interleave_bytes: parts of about this size.
+constexpr uint64_t kQueuePartBytes = 256 * 1024;
 // CTA shares are cut at multiples of 512 bytes from a piece's start, so that a
 // warp's 32 x 16-byte vectors cover whole 128-byte lines and 32-byte sectors
 // (a cut at 16 bytes leaves every warp straddling one extra line and two
@@ -131,6 +133,7 @@ Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
   t.stages = 3;
   t.store_hint = 1;
   t.min_cta_bytes = 512;
+  t.schedule = kSchedItem;
   switch (coll) {
     case kAllReduce:
     case kAtomReduce:
@@ -231,6 +234,7 @@ Tune tune_merge(const Tune& b, const Tune& o) {
   if (o.min_cta_bytes) t.min_cta_bytes = o.min_cta_bytes;
   if (o.interleave_bytes) t.interleave_bytes = o.interleave_bytes;
   if (o.max_ctas) t.max_ctas = o.max_ctas;
+  if (o.schedule) t.schedule = o.schedule;
   return t;
 }
 
@@ -247,6 +251,7 @@ static int validate_tune(const Tune& t) {
   if (t.interleave_bytes < -1 || (t.interleave_bytes > 0 && (t.interleave_bytes < 512 || t.interleave_bytes % 512)))
     return PL_ERR_INVALID_ARG;
   if (t.max_ctas < 0) return PL_ERR_INVALID_ARG;
+  if (t.schedule < kSchedItem || t.schedule > kSchedQueue) return PL_ERR_INVALID_ARG;
   return PL_OK;
 }
 
@@ -467,6 +472,8 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
     }
   }
   if (!p.reduce) p.nsrc = 1;
+  // streamed schedules run copy plans on the bulk path only
+  if (p.tune.schedule != kSchedItem && (p.reduce || sync || p.tune.path != kPathBulk)) return PL_ERR_UNSUPPORTED;
 
   // ------------------------------------------------------------ tiling
   uint64_t gcap = (uint64_t)p.tune.ctas_per_sm * (uint64_t)sm_count;
@@ -487,19 +494,24 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
     // nparts = k * grid with parts of about T bytes, and CTA c takes parts
     // c, c + grid, c + 2 grid, ... in that order: at any moment the CTAs work
     // on neighbouring parts, and every CTA still gets the same number of bytes.
+    // The queue schedule cuts the same parts (of interleave_bytes, else about
+    // kQueuePartBytes) but keeps them in one list in global order; CTAs take
+    // the next item from a shared counter, so faster CTAs take more.
     uint64_t W = 0;
     for (const Piece& q : pieces) W += q.len;
     uint64_t G = std::max<uint64_t>(1, std::min<uint64_t>(gcap, ceil_div(W, (uint64_t)p.tune.min_cta_bytes)));
     // shares of at least one 512-byte granule, except that pieces smaller than
     // that may each get a CTA of their own (latency of small calls)
     G = std::min<uint64_t>(G, std::max<uint64_t>({1, W / kSplitGranule, (uint64_t)pieces.size()}));
+    const bool queue = p.tune.schedule == kSchedQueue;
     uint64_t k = 1;
-    if (p.tune.interleave_bytes > 0) {
-      const uint64_t T = (uint64_t)p.tune.interleave_bytes;
+    if (p.tune.interleave_bytes > 0 || queue) {
+      const uint64_t T = p.tune.interleave_bytes > 0 ? (uint64_t)p.tune.interleave_bytes : kQueuePartBytes;
       k = std::max<uint64_t>(1, (W + T * G / 2) / (T * G));
       k = std::min<uint64_t>(k, std::max<uint64_t>(1, W / (kSplitGranule * G)));
     }
     const uint64_t nparts = k * G;
+    p.queue = queue;
     p.grid = (int)G;
     std::vector<uint64_t> start(pieces.size() + 1, 0);
     for (size_t i = 0; i < pieces.size(); ++i) start[i + 1] = start[i] + pieces[i].len;
@@ -527,7 +539,8 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
         const uint64_t b = (uint64_t)(((unsigned __int128)(j + 1) * W) / nparts);
         locate(b, ep, eo);
       }
-      std::vector<Item>& dst = per_cta[(size_t)(j % G)];
+      // the shared queue hands out items in global order: one list
+      std::vector<Item>& dst = per_cta[queue ? 0 : (size_t)(j % G)];
       while (cp < ep || (cp == ep && co < eo)) {
         const Piece& q = pieces[cp];
         const uint64_t end = (cp == ep) ? eo : q.len;

@@ -40,6 +40,13 @@ enum Layout : int { kLayoutAuto = 0, kOneShot = 1, kTwoShot = 2 };
 
 enum Path : int { kPathRegister = 1, kPathBulk = 2 };
 
+// How a CTA walks its work.  Item: one item at a time (each bulk item fills
+// and drains its own pipeline).  Stream: a CTA's items flow through one
+// continuous bulk pipeline.  Queue: streamed, and the CTAs take items in
+// order from a counter shared by the grid instead of fixed shares.  Stream
+// and queue serve copy plans on the bulk path.
+enum Schedule : int { kSchedItem = 1, kSchedStream = 2, kSchedQueue = 3 };
+
 // Device format of one work item (40 bytes).  Same field meanings as
 // purlin_item in the public header, minus the CTA bookkeeping.
 struct Item {
@@ -65,6 +72,7 @@ struct Tune {
   int min_cta_bytes = 0;
   int interleave_bytes = 0;  // > 0: parts of about this size, CTA c takes parts c, c + grid, ...
   int max_ctas = 0;          // > 0: cap on the grid size
+  int schedule = 0;          // Schedule
 };
 
 struct Plan {
@@ -76,6 +84,7 @@ struct Plan {
   std::vector<uint32_t> cta_begin;  // contiguous assignment: grid + 1 entries
   bool strided = false;      // item i runs on CTA i % grid, in increasing i
   bool sync = false;         // items wait on / notify SNAC flags (CTAs must be co-resident)
+  bool queue = false;        // CTAs take items from the shared queue (items in global order)
   int grid = 0;
   int n_flags = 0;           // SNAC flags used (two-shot layout)
   uint64_t in_bytes[kMaxWorld] = {};   // bytes each input must hold

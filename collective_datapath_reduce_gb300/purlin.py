@@ -41,6 +41,7 @@ PL_COLL_ATOM_REDUCE = 8
 
 PL_LAYOUT_AUTO, PL_LAYOUT_ONE_SHOT, PL_LAYOUT_TWO_SHOT = 0, 1, 2
 PATH_REGISTER, PATH_BULK = 1, 2
+PL_SCHED_ITEM, PL_SCHED_STREAM, PL_SCHED_QUEUE = 1, 2, 3
 
 MAX_WORLD = 16
 
@@ -55,7 +56,7 @@ class PurlinError(RuntimeError):
 class purlin_tune(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "layout", "ctas_per_sm", "threads", "unroll", "path", "chunk_bytes", "stages",
-        "store_hint", "min_cta_bytes", "interleave_bytes", "max_ctas")]
+        "store_hint", "min_cta_bytes", "interleave_bytes", "max_ctas", "schedule")]
 
 
 class purlin_item(ctypes.Structure):

@@ -110,7 +110,19 @@ typedef struct {
                            this size and CTA c takes parts c, c + grid, ...; -1: one
                            contiguous share per CTA (0 = the table's choice) */
   int max_ctas;     /* > 0: at most this many CTAs (fewer concurrent DRAM streams) */
+  int schedule;     /* purlin_schedule: how CTAs walk their items */
 } purlin_tune;
+
+/* How the CTAs of a launch walk the plan's work items (purlin_tune.schedule).
+ * PL_SCHED_ITEM: each CTA runs its own share one item at a time (on the bulk
+ * path every item fills and drains its own pipeline).  PL_SCHED_STREAM: a
+ * CTA's items flow through one continuous bulk pipeline.  PL_SCHED_QUEUE:
+ * streamed, and CTAs take items in order from a counter the grid shares
+ * (the plan's parts are about interleave_bytes, else 256 KiB), so CTAs that
+ * get more DRAM bandwidth take more items.  STREAM and QUEUE serve copy
+ * collectives on the bulk path (path = 2); elsewhere they return
+ * PL_ERR_UNSUPPORTED. */
+typedef enum { PL_SCHED_ITEM = 1, PL_SCHED_STREAM = 2, PL_SCHED_QUEUE = 3 } purlin_schedule;
 
 /* One work item of a plan, as purlin_plan_describe reports it. */
 typedef struct {
@@ -122,8 +134,8 @@ typedef struct {
   uint32_t dst_mask; /* bit r: output of rank r */
   uint32_t wait;     /* 0, or 1 + index of the SNAC flag consumed before the item */
   uint32_t notify;   /* 0, or 1 + index of the SNAC flag raised after the item */
-  uint32_t cta;      /* CTA that runs the item */
-  uint32_t order;    /* position of the item in that CTA's sequence */
+  uint32_t cta;      /* CTA that runs the item; 0xFFFFFFFF under PL_SCHED_QUEUE (any CTA) */
+  uint32_t order;    /* position of the item in that CTA's sequence (in the queue) */
 } purlin_item;
 
 /* ---------------------------------------------------------------- set-up */

@@ -227,3 +227,57 @@ def test_interleaved_plans(interleave):
         assert np.array_equal(outs[r], want[r])
     st, *_ = P.purlin_plan_describe(P.PL_COLL_ALL_GATHER, 2, P.PL_U8, [64], tune={"interleave_bytes": 100})
     assert st == P.PL_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("part", [0, 4096, 65536])
+def test_queue_plans(part):
+    """Queue schedule: items in global order (part after part), same coverage as
+    the static plan, every item taken by whichever CTA asks (cta = 0xFFFFFFFF)."""
+    tune = {"path": P.PATH_BULK, "schedule": P.PL_SCHED_QUEUE, "interleave_bytes": part}
+    world = 8
+    C = RNG.integers(0, 60000, size=(world, world))
+    C[0, 1] = 0
+    sres, dres = _res(world, False), _res(world, False)
+    src_addr = [0x1000000 * (r + 1) + sres[r] for r in range(world)]
+    dst_addr = [0x9000000 * (r + 1) + dres[r] for r in range(world)]
+    st, items, grid, nflags = P.purlin_plan_describe(P.PL_COLL_ALL_TO_ALL_V, world, P.PL_U8, C.reshape(-1).tolist(),
+                                                     src_addr, dst_addr, 152, tune)
+    assert st == P.PL_OK and nflags == 0 and 1 <= grid <= 2 * 152
+    assert [it["order"] for it in items] == list(range(len(items)))
+    assert all(it["cta"] == 0xFFFFFFFF for it in items)
+    T = part or 256 * 1024
+    total = int(C.sum())
+    assert len(items) >= min(grid, total // T)
+    assert max(it["len"] for it in items) <= max(2 * T, total // grid + 512)
+    # global order: each destination's bytes appear in ascending offset order
+    last = {}
+    for it in items:
+        key = it["dst_mask"]
+        assert it["dst_off"] >= last.get(key, 0)
+        last[key] = it["dst_off"] + it["len"]
+    ins = [RNG.integers(0, 256, size=int(C[s].sum()), dtype=np.uint8) for s in range(world)]
+    outs = [np.zeros(int(C[:, d].sum()), np.uint8) for d in range(world)]
+    run_items(items, ins, outs, "u8")
+    want = oracle.all_to_all_v(ins, C)
+    for r in range(world):
+        assert np.array_equal(outs[r], want[r])
+
+
+def test_streamed_schedules_need_bulk_copies():
+    """Stream and queue schedules serve copy plans on the bulk path only."""
+    for sched in (P.PL_SCHED_STREAM, P.PL_SCHED_QUEUE):
+        st, *_ = P.purlin_plan_describe(P.PL_COLL_ALL_GATHER, 4, P.PL_U8, [1 << 20],
+                                        tune={"path": P.PATH_BULK, "schedule": sched})
+        assert st == P.PL_OK
+        st, *_ = P.purlin_plan_describe(P.PL_COLL_ALL_GATHER, 4, P.PL_U8, [1 << 20],
+                                        tune={"path": P.PATH_REGISTER, "schedule": sched})
+        assert st == P.PL_ERR_UNSUPPORTED
+        st, *_ = P.purlin_plan_describe(P.PL_COLL_REDUCE_SCATTER, 4, P.PL_F32, [1 << 20],
+                                        tune={"path": P.PATH_BULK, "schedule": sched})
+        assert st == P.PL_ERR_UNSUPPORTED
+        st, *_ = P.purlin_plan_describe(P.PL_COLL_ALL_REDUCE, 4, P.PL_F32, [1 << 20],
+                                        tune={"path": P.PATH_BULK, "schedule": sched,
+                                              "layout": P.PL_LAYOUT_TWO_SHOT})
+        assert st == P.PL_ERR_UNSUPPORTED
+    st, *_ = P.purlin_plan_describe(P.PL_COLL_ALL_GATHER, 4, P.PL_U8, [1 << 20], tune={"schedule": 4})
+    assert st == P.PL_ERR_INVALID_ARG
