@@ -109,16 +109,21 @@ size_t n_sizes(int coll, int world) {
 //   ReduceScatter  from 8 MiB per rank the TMA bulk ring (2 slots x 32 KiB
 //               per source) runs above the copy bandwidth: the traffic is
 //               8 reads per write.  Below that, the register path.
-//   AllGather   from 4 MiB per rank register copies on 128 CTAs of 512
-//               threads with evict-first stores (6457 GB/s at 8 x 256 MiB
-//               against 6345 for the bulk ring); AllGatherV (misaligned
-//               pieces) the bulk ring with 32 KiB chunks on 128 CTAs.  Below,
-//               register copies.
-//   AllToAll    from 32 MiB per rank the bulk ring (3 x 32 KiB); below,
-//               register copies with streaming stores.
-//   Copy Atom, one destination: from 32 MiB the bulk ring with no grid cap
-//               (6015 against 5192 GB/s for the AllGather setting at 256 MiB,
-//               6667 against 5513 at 1 GiB); from 4 MiB, 8 vectors per thread.
+//   AllGather   from 16 MiB per rank the streamed bulk ring fed from the
+//               shared item queue in 16 KiB parts (6904 against 6466 GB/s for
+//               register copies at 8 x 256 MiB, 6529 against 6254 at 16 MiB);
+//               from 4 MiB register copies on 128 CTAs of 512 threads with
+//               evict-first stores (5756 against 5646 at 4 MiB).  AllGatherV
+//               (misaligned pieces): the queue in 32 KiB parts on 128 CTAs
+//               (5889 against 5681 item by item).
+//   AllToAll    from 16 MiB per rank the queue in 64 KiB parts, 5 slots (7096
+//               against 6864 item by item at 256 MiB, 6800 against 6557 at 64
+//               MiB); AllToAllV from 32 MiB the queue in 192 KiB parts, 4
+//               slots (5923 against 5768).  Below, register copies with
+//               streaming stores.
+//   Copy Atom, one destination: from 32 MiB the queue in 64 KiB parts (6973
+//               against 6762 GB/s item by item at 1 GiB); from 4 MiB, 8
+//               vectors per thread.
 Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
   (void)dtype;
   const uint64_t S = bytes_per_rank;
@@ -165,11 +170,13 @@ Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
     case kAtomCopy:
       if (coll == kAtomCopy && world == 1 && S >= 4 * MiB) {
         // one destination: one store per load, so more bytes in flight per
-        // thread; from 32 MiB the bulk ring, one CTA per SM, no grid cap
+        // thread; from 32 MiB the bulk ring fed from the shared queue
         if (S >= 32 * MiB) {
           t.path = kPathBulk;
           t.ctas_per_sm = 1;
-          t.stages = 3;
+          t.stages = 4;
+          t.schedule = kSchedQueue;
+          t.interleave_bytes = 64 * 1024;
         } else {
           t.threads = 512;
           t.unroll = 8;
@@ -177,13 +184,24 @@ Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
           t.store_hint = 2;
         }
       } else if (S >= 4 * MiB && coll == kAllGatherV) {
-        // AllGatherV pieces are mostly misaligned: shifted bulk copies, which
-        // amortise better over large chunks
+        // AllGatherV pieces are mostly misaligned: shifted bulk copies from
+        // the shared queue in 32 KiB parts, 128 CTAs
         t.path = kPathBulk;
         t.ctas_per_sm = 1;
         t.max_ctas = 128;
-        t.stages = 4;
+        t.stages = 3;
         t.chunk_bytes = 32 * 1024;
+        t.schedule = kSchedQueue;
+        t.interleave_bytes = 32 * 1024;
+      } else if (S >= 16 * MiB && coll == kAllGather) {
+        // one bulk load, eight bulk stores per chunk; 16 KiB parts from the
+        // shared queue, one CTA per SM
+        t.path = kPathBulk;
+        t.ctas_per_sm = 1;
+        t.stages = 3;
+        t.chunk_bytes = 32 * 1024;
+        t.schedule = kSchedQueue;
+        t.interleave_bytes = 16 * 1024;
       } else if (S >= 4 * MiB) {
         // one load, eight stores per vector: like the AllReduce, 128 CTAs of
         // 512 threads with evict-first stores
@@ -197,11 +215,22 @@ Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
       break;
     case kAllToAll:
     case kAllToAllV:
-      if (S >= 32 * MiB) {
+      if (coll == kAllToAllV && S >= 32 * MiB) {
+        // mostly misaligned pieces: shifted bulk copies from the shared queue
         t.path = kPathBulk;
         t.ctas_per_sm = 1;
-        t.stages = 3;
+        t.stages = 4;
         t.chunk_bytes = 32 * 1024;
+        t.schedule = kSchedQueue;
+        t.interleave_bytes = 192 * 1024;
+      } else if (coll == kAllToAll && S >= 16 * MiB) {
+        // bulk ring of 5 slots fed from the shared queue in 64 KiB parts
+        t.path = kPathBulk;
+        t.ctas_per_sm = 1;
+        t.stages = 5;
+        t.chunk_bytes = 32 * 1024;
+        t.schedule = kSchedQueue;
+        t.interleave_bytes = 64 * 1024;
       } else {
         t.unroll = 2;
         t.store_hint = 2;
