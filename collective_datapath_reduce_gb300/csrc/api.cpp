@@ -318,9 +318,15 @@ purlin_status run(purlin_ctx* h, int coll, int world, int dtype, const uint64_t*
   if (d->plan.sync) {
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+  } else {
+    // programmatic dependent launch: the launch may start once the previous
+    // kernel on the stream has retired its CTAs; the kernel waits for that
+    // grid's completion (grid_dep_wait) before it touches memory
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
   }
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   void* args[] = {&a};
   cudaError_t e = cudaLaunchKernelExC(&cfg, d->fn, args);
   if (e != cudaSuccess) {

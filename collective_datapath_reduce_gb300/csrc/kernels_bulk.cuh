@@ -331,6 +331,7 @@ __global__ void __launch_bounds__(512, 1) bulk_kernel(const __grid_constant__ KA
   __shared__ int s_ns, s_nd, s_ok, s_aligned;
   __shared__ uint32_t s_notify, s_epoch, s_wait_ns;
   __shared__ unsigned long long s_t0;
+  grid_dep_wait();
 
   const int stages = a.stages;
   const uint32_t ch = a.chunk_bytes;

@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(512, 1) stream_copy_kernel(const __grid_consta
   __shared__ uint64_t full[8];
   __shared__ StreamItem SI[kItemRing];
   __shared__ StreamChunk SC[8];
+  grid_dep_wait();
 
   const uint32_t stages = (uint32_t)a.stages;
   const uint32_t ch = a.chunk_bytes;
