@@ -48,6 +48,7 @@ struct purlin_ctx {
   int sm_count = 0;
   int arch = 0;
   int max_ctas_per_sm = 0;
+  int pageable_access = 0;   // the device can address pageable host memory
   void* ws = nullptr;
   size_t ws_bytes = 0;
   bool ws_owned = false;
@@ -160,10 +161,11 @@ purlin_status ensure_flags(purlin_ctx* h, size_t need, cudaStream_t stream) {
 }
 
 std::string plan_key(int coll, int world, int dtype, const uint64_t* sizes, size_t n,
-                     const uint8_t* sres, const uint8_t* dres, const purlin_ctx* h) {
+                     const uint8_t* sres, const uint8_t* dres, bool host_mem, const purlin_ctx* h) {
   std::string k;
   k.reserve(64 + n * 8);
   auto put = [&](const void* p, size_t b) { k.append((const char*)p, b); };
+  put(&host_mem, sizeof host_mem);
   put(&coll, sizeof coll);
   put(&world, sizeof world);
   put(&dtype, sizeof dtype);
@@ -175,15 +177,22 @@ std::string plan_key(int coll, int world, int dtype, const uint64_t* sizes, size
 }
 
 purlin_status get_plan(purlin_ctx* h, int coll, int world, int dtype, const uint64_t* sizes, size_t n,
-                       const uint8_t* sres, const uint8_t* dres, cudaStream_t stream, DevPlan** out) {
-  const std::string key = plan_key(coll, world, dtype, sizes, n, sres, dres, h);
+                       const uint8_t* sres, const uint8_t* dres, bool host_mem, cudaStream_t stream,
+                       DevPlan** out) {
+  const std::string key = plan_key(coll, world, dtype, sizes, n, sres, dres, host_mem, h);
   auto it = h->plans.find(key);
   if (it != h->plans.end()) {
     *out = it->second.get();
     return PL_OK;
   }
   auto d = std::make_unique<DevPlan>();
-  const pl::Tune over = h->has_over ? h->over : pl::Tune{};
+  pl::Tune over = h->has_over ? h->over : pl::Tune{};
+  if (host_mem) {
+    // buffers in host memory: register path, item by item (the bulk copy
+    // engines are kept to device memory)
+    over.path = pl::kPathRegister;
+    over.schedule = pl::kSchedItem;
+  }
   int st = pl::build_plan(coll, world, dtype, sizes, n, sres, dres, h->sm_count, 0, over, &d->plan);
   if (st) return (purlin_status)st;
   d->fn = pick_kernel(d->plan);
@@ -268,20 +277,61 @@ purlin_status get_plan(purlin_ctx* h, int coll, int world, int dtype, const uint
 }
 
 // Plan (cached) and launch one call.  in/out: `nin` / `nout` buffer pointers.
+// Where one rank buffer lives, and the address the kernel uses for it.
+// Device and managed memory take every path.  Host memory the device maps
+// (cudaHostAlloc, cudaHostRegister) is read and written in place over the
+// host link; pageable host memory only where the device can address it.
+// Anything else (another device's memory, an unknown address) is refused.
+purlin_status locate(const purlin_ctx* h, const void* p, const void** dev_p, bool* host) {
+  *dev_p = p;
+  if (!p) return PL_OK;  // a zero-byte rank of a V collective
+  cudaPointerAttributes at;
+  cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return PL_ERR_INVALID_ARG;
+  }
+  switch (at.type) {
+    case cudaMemoryTypeDevice:
+      return at.device == h->device ? PL_OK : PL_ERR_INVALID_ARG;
+    case cudaMemoryTypeManaged:
+      return PL_OK;
+    case cudaMemoryTypeHost:
+      if (at.devicePointer) *dev_p = at.devicePointer;
+      *host = true;
+      return PL_OK;
+    default:  // unregistered host memory
+      if (!h->pageable_access) return PL_ERR_INVALID_ARG;
+      *host = true;
+      return PL_OK;
+  }
+}
+
 purlin_status run(purlin_ctx* h, int coll, int world, int dtype, const uint64_t* sizes, size_t n,
-                  const void* const* in, int nin, void* const* out, int nout, cudaStream_t stream) {
-  uint8_t sres[pl::kMaxWorld] = {}, dres[pl::kMaxWorld] = {};
-  for (int r = 0; r < nin; ++r) sres[r] = (uint8_t)((uintptr_t)in[r] & 15u);
-  for (int r = 0; r < nout; ++r) dres[r] = (uint8_t)((uintptr_t)out[r] & 15u);
+                  const void* const* in_arg, int nin, void* const* out_arg, int nout, cudaStream_t stream) {
   // The workspace and the plans live on the device that was current when the
   // handle was created; launching with another device current would hand the
   // kernel pointers of a different GPU.
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess) return cuda_fail(cudaErrorInvalidDevice);
   if (cur != h->device) return PL_ERR_INVALID_ARG;
+  const void* in[pl::kMaxWorld] = {};
+  void* out[pl::kMaxWorld] = {};
+  bool host_mem = false;
+  purlin_status st;
+  for (int r = 0; r < nin; ++r)
+    if ((st = locate(h, in_arg[r], &in[r], &host_mem))) return st;
+  for (int r = 0; r < nout; ++r) {
+    const void* q = nullptr;
+    if ((st = locate(h, out_arg[r], &q, &host_mem))) return st;
+    out[r] = const_cast<void*>(q);
+  }
+  uint8_t sres[pl::kMaxWorld] = {}, dres[pl::kMaxWorld] = {};
+  for (int r = 0; r < nin; ++r) sres[r] = (uint8_t)((uintptr_t)in[r] & 15u);
+  for (int r = 0; r < nout; ++r) dres[r] = (uint8_t)((uintptr_t)out[r] & 15u);
   std::lock_guard<std::mutex> lock(h->mu);
   DevPlan* d = nullptr;
-  purlin_status st = get_plan(h, coll, world, dtype, sizes, n, sres, dres, stream, &d);
+  st = get_plan(h, coll, world, dtype, sizes, n, sres, dres, host_mem, stream, &d);
   if (st) return st;
   if (d->plan.items.empty()) return PL_OK;
   if ((st = ensure_flags(h, (size_t)d->plan.n_flags, stream))) return st;
@@ -412,6 +462,8 @@ purlin_status purlin_initialize(int world, void* workspace, size_t workspace_byt
       (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, h->device)) != cudaSuccess)
     return cuda_fail(e);
   h->arch = major * 10 + minor;
+  if ((e = cudaDeviceGetAttribute(&h->pageable_access, cudaDevAttrPageableMemoryAccess, h->device)) != cudaSuccess)
+    return cuda_fail(e);
   const void* probe = pl::kernel_reduce_bf16(8, 1);
   if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&h->max_ctas_per_sm, probe, 512, 0)) != cudaSuccess)
     return cuda_fail(e);

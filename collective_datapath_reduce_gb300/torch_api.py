@@ -53,8 +53,8 @@ def _same(tensors, world, what):
     if len(tensors) != world:
         raise ValueError(f"{what}: expected {world} tensors (one per rank), got {len(tensors)}")
     for t in tensors:
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{what}: tensors must be contiguous CUDA tensors")
+        if not (t.is_cuda or t.is_pinned()) or not t.is_contiguous():
+            raise ValueError(f"{what}: tensors must be contiguous CUDA tensors or pinned host tensors")
 
 
 def initialize(world: int, device=None, stream=None) -> Handle:
