@@ -440,50 +440,52 @@ def side_table(P, h, stream, dev):
     """The metric against size: GB/s (algorithmic bytes) and microseconds per
     call for every collective over the workloads' size range, the two-shot
     AllReduce layout, the two Atoms, and the device-to-device copy of the same
-    traffic.  Each library point is one CUDA graph of 10 calls (the pages'
-    graphLaunches knob) replayed after warm-up, timed with events; the copy
-    reference is 10 plain launches of torch's copy kernel."""
+    traffic.  Each library point is a CUDA graph of 10 calls (the pages'
+    graphLaunches knob): 5 warm-up replays, then 20 timed replays, each after
+    a write of twice the L2 size; the point gives the median and the 10th /
+    90th percentiles of the time per call.  Points whose working set fits in
+    the L2 are marked: after the first call of a replay they run from the L2.
+    The copy reference is 10 plain launches of torch's copy kernel."""
     import torch
     gen = torch.Generator(device=dev)
     gen.manual_seed(7)
-    GRAPH = 10
+    GRAPH, WARM, RUNS = 10, 5, 20
     MI = 1 << 20
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * MI))
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
 
-    def timeit(fn, reps=3, graph=True):
+    def timeit(fn, graph=True):
+        """Per-call milliseconds of each timed run."""
         with torch.cuda.stream(stream):
             for _ in range(3):
                 fn()
             stream.synchronize()
-            if not graph:
-                best = None
-                for _ in range(reps):
-                    a = torch.cuda.Event(enable_timing=True)
-                    b = torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
+            g = None
+            if graph:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
                     for _ in range(GRAPH):
                         fn()
-                    b.record(stream)
-                    stream.synchronize()
-                    ms = a.elapsed_time(b) / GRAPH
-                    best = ms if best is None else min(best, ms)
-                return best
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for _ in range(GRAPH):
-                    fn()
-            g.replay()
-            best = None
-            for _ in range(reps):
+            def run():
+                if g is not None:
+                    g.replay()
+                else:
+                    for _ in range(GRAPH):
+                        fn()
+            for _ in range(WARM):
+                run()
+            times = []
+            for k in range(RUNS):
+                flush.fill_(k & 0xFF)
                 a = torch.cuda.Event(enable_timing=True)
                 b = torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-                g.replay()
+                run()
                 b.record(stream)
                 stream.synchronize()
-                ms = a.elapsed_time(b) / GRAPH
-                best = ms if best is None else min(best, ms)
+                times.append(a.elapsed_time(b) / GRAPH)
             del g
-            return best
+            return times
 
     def bufs(n, count, dtype=torch.uint8):
         if dtype == torch.uint8:
@@ -491,8 +493,16 @@ def side_table(P, h, stream, dev):
                     for _ in range(count)]
         return [torch.randn(max(n, 1), dtype=dtype, device=dev, generator=gen) for _ in range(count)]
 
-    def point(nbytes, ms):
-        return {"bytes": nbytes, "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms / 1e3) / 1e9, 1)}
+    def point(nbytes, times):
+        # the algorithmic bytes are the distinct bytes a call touches: its working set
+        t = sorted(times)
+        med = statistics.median(t)
+        pct = lambda q: t[min(len(t) - 1, int(q * (len(t) - 1) + 0.5))]
+        d = {"bytes": nbytes, "us": round(med * 1e3, 2), "us_p10": round(pct(0.1) * 1e3, 2),
+             "us_p90": round(pct(0.9) * 1e3, 2), "GB/s": round(nbytes / (med / 1e3) / 1e9, 1)}
+        if nbytes <= l2:
+            d["l2_resident"] = True
+        return d
 
     out = {"d2d_copy": {}, "all_gather_u8": {}, "all_to_all_u8": {}, "all_reduce_bf16": {},
            "reduce_scatter_f32": {}, "all_reduce_two_shot_bf16": {}, "reduce_scatter_v_bf16": {},
@@ -563,10 +573,10 @@ def side_table(P, h, stream, dev):
         g = EX.max_grid()
         f.coll_blocks = g
         f.status = status.data_ptr()
-        ms = timeit(lambda: EX.launch(f, g, stream.cuda_stream), graph=False)
+        times = timeit(lambda: EX.launch(f, g, stream.cuda_stream), graph=False)
         if int(status.item()) != 0:
             raise RuntimeError("device-side collective reported a time-out")
-        out["device_api_fused"][nm] = point(alg, ms)
+        out["device_api_fused"][nm] = point(alg, times)
         del src, dst
     torch.cuda.empty_cache()
     for size in (64 * MI, 256 * MI):
