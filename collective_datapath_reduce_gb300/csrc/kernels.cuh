@@ -95,18 +95,31 @@ __device__ __forceinline__ void run_item(const char* const* src, int ns, char* c
   }
 }
 
+// Items of a CTA: its contiguous range, every grid-th item (strided SNAC
+// plans), or, with the shared queue (`a.queue`), item blockIdx.x first and
+// then whatever index the grid-wide counter hands out next.  Every item an
+// item waits on comes earlier in the global order, and a CTA only holds (in
+// its prefetch registers) an index larger than the one it runs, so the
+// earliest unfinished item is always running and the queue cannot deadlock
+// a SNAC plan (all CTAs are resident: cooperative launch).
 template <typename T, int NS, int U>
 __global__ void __launch_bounds__(512, 2) snac_kernel(const __grid_constant__ KArgs a) {
+  constexpr uint32_t kNoItem = 0xFFFFFFFFu;
   __shared__ const char* s_src[kMaxWorld];
   __shared__ char* s_dst[kMaxWorld];
   __shared__ uint64_t s_len;
   __shared__ int s_ns, s_nd, s_ok;
-  __shared__ uint32_t s_notify, s_epoch, s_wait_ns;
+  __shared__ uint32_t s_item, s_notify, s_epoch, s_wait_ns;
+  __shared__ uint32_t s_next_i, s_q_i;  // thread 0's item cursor (kept out of the registers of the Atoms)
   __shared__ unsigned long long s_t0;
   grid_dep_wait();
 
   uint32_t begin, end, step;
-  if (a.strided) {
+  if (a.queue) {
+    begin = blockIdx.x;
+    end = a.n_items;
+    step = 0;
+  } else if (a.strided) {
     begin = blockIdx.x;
     end = a.n_items;
     step = gridDim.x;
@@ -117,33 +130,52 @@ __global__ void __launch_bounds__(512, 2) snac_kernel(const __grid_constant__ KA
   }
   if (threadIdx.x == 0) s_epoch = a.sync ? ld_volatile(&a.ctl[kCtlEpoch]) + 1u : 0u;
 
-  // Thread 0 keeps the next item in registers so its load overlaps the current one.
+  // Thread 0 keeps the next item in registers so its load overlaps the
+  // current one (and, on the queue, the index fetched for the item after it).
   Item next;
-  if (threadIdx.x == 0 && begin < end) next = a.items[begin];
-  for (uint32_t i = begin; i < end; i += step) {
+  if (threadIdx.x == 0) {
+    s_next_i = begin;
+    s_q_i = 0;
+    if (begin < end) {
+      next = a.items[begin];
+      if (a.queue) s_q_i = gridDim.x + atomicAdd(&a.ctl[kCtlQueue], 1u);
+    }
+  }
+  for (;;) {
     if (threadIdx.x == 0) {
-      const Item it = next;
-      if (i + step < end) next = a.items[i + step];
-      int ns = 0, nd = 0;
-      for (uint32_t m = it.src_mask; m; m &= m - 1) {
-        const int b = __ffs(m) - 1;
-        s_src[ns++] = (b < 16 ? a.in[b] : a.out[b - 16]) + it.src_off;
+      s_item = kNoItem;
+      const uint32_t i = s_next_i;
+      if (i < end) {
+        const Item it = next;
+        const uint32_t ni = a.queue ? s_q_i : i + step;
+        s_next_i = ni;
+        if (ni < end) {
+          next = a.items[ni];
+          if (a.queue) s_q_i = gridDim.x + atomicAdd(&a.ctl[kCtlQueue], 1u);
+        }
+        s_item = i;
+        int ns = 0, nd = 0;
+        for (uint32_t m = it.src_mask; m; m &= m - 1) {
+          const int b = __ffs(m) - 1;
+          s_src[ns++] = (b < 16 ? a.in[b] : a.out[b - 16]) + it.src_off;
+        }
+        for (uint32_t m = it.dst_mask; m; m &= m - 1) s_dst[nd++] = a.out[__ffs(m) - 1] + it.dst_off;
+        s_ns = ns;
+        s_nd = nd;
+        s_len = it.len;
+        s_notify = it.notify;
+        int ok = 1;
+        const unsigned long long t0 = a.trace ? globaltimer() : 0ull;
+        if (it.wait) ok = consume_wait(a, a.flags + (it.wait - 1), s_epoch);
+        s_t0 = t0;
+        s_wait_ns = a.trace ? (uint32_t)min(globaltimer() - t0, 0xFFFFFFFFull) : 0u;
+        if (a.sync && ok && ld_volatile(&a.ctl[kCtlStatus]) != 0) ok = 0;
+        s_ok = ok;
       }
-      for (uint32_t m = it.dst_mask; m; m &= m - 1) s_dst[nd++] = a.out[__ffs(m) - 1] + it.dst_off;
-      s_ns = ns;
-      s_nd = nd;
-      s_len = it.len;
-      s_notify = it.notify;
-      int ok = 1;
-      const unsigned long long t0 = a.trace ? globaltimer() : 0ull;
-      if (it.wait) ok = consume_wait(a, a.flags + (it.wait - 1), s_epoch);
-      s_t0 = t0;
-      s_wait_ns = a.trace ? (uint32_t)min(globaltimer() - t0, 0xFFFFFFFFull) : 0u;
-      if (a.sync && ok && ld_volatile(&a.ctl[kCtlStatus]) != 0) ok = 0;
-      s_ok = ok;
     }
     __syncthreads();
-    if (!s_ok) break;
+    const uint32_t i = s_item;
+    if (i == kNoItem || !s_ok) break;
     if (a.store_hint == 2)
       run_item<T, NS, U, true>(s_src, s_ns, s_dst, s_nd, s_len);
     else
@@ -158,7 +190,9 @@ __global__ void __launch_bounds__(512, 2) snac_kernel(const __grid_constant__ KA
     }
   }
   if (a.sync) {
-    // The last CTA to finish publishes the launch's epoch for the next one.
+    // The last CTA to finish publishes the launch's epoch for the next one
+    // (and resets the queue: every CTA made its last fetch before counting
+    // itself done).
     __syncthreads();
     if (threadIdx.x == 0) {
       __threadfence();
@@ -166,6 +200,17 @@ __global__ void __launch_bounds__(512, 2) snac_kernel(const __grid_constant__ KA
       if (done == gridDim.x - 1) {
         a.ctl[kCtlDone] = 0u;
         a.ctl[kCtlEpoch] = s_epoch;
+        if (a.queue) a.ctl[kCtlQueue] = 0u;
+        __threadfence();
+      }
+    }
+  } else if (a.queue) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      if (atomicAdd(&a.ctl[kCtlQueueDone], 1u) == gridDim.x - 1) {
+        a.ctl[kCtlQueue] = 0u;
+        a.ctl[kCtlQueueDone] = 0u;
         __threadfence();
       }
     }

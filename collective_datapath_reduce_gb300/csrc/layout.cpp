@@ -501,8 +501,10 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
     }
   }
   if (!p.reduce) p.nsrc = 1;
-  // streamed schedules run copy plans on the bulk path only
-  if (p.tune.schedule != kSchedItem && (p.reduce || sync || p.tune.path != kPathBulk)) return PL_ERR_UNSUPPORTED;
+  // Streamed schedules are copy plans on the bulk path.  The shared queue
+  // serves every plan on the register path, and copy plans on the bulk path.
+  if (p.tune.schedule == kSchedStream && (p.reduce || sync || p.tune.path != kPathBulk)) return PL_ERR_UNSUPPORTED;
+  if (p.tune.schedule == kSchedQueue && p.tune.path == kPathBulk && (p.reduce || sync)) return PL_ERR_UNSUPPORTED;
 
   // ------------------------------------------------------------ tiling
   uint64_t gcap = (uint64_t)p.tune.ctas_per_sm * (uint64_t)sm_count;
@@ -510,6 +512,7 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
   if (sync) {
     p.strided = true;
     p.sync = true;
+    p.queue = p.tune.schedule == kSchedQueue;
     p.n_flags = (int)n_flags;
     const uint64_t n = pieces.size();
     p.grid = (int)std::max<uint64_t>(1, std::min<uint64_t>(gcap, n));

@@ -125,8 +125,11 @@ typedef struct {
  * CTA's items flow through one continuous bulk pipeline.  PL_SCHED_QUEUE:
  * streamed, and CTAs take items in order from a counter the grid shares
  * (the plan's parts are about interleave_bytes, else 256 KiB), so CTAs that
- * get more DRAM bandwidth take more items.  STREAM and QUEUE serve copy
- * collectives on the bulk path (path = 2); elsewhere they return
+ * get more DRAM bandwidth take more items.  STREAM serves copy collectives on
+ * the bulk path (path = 2).  QUEUE serves every collective on the register
+ * path (path = 1; two-shot SNAC plans included: an item only waits on
+ * earlier items, so the earliest unfinished item always runs) and copy
+ * collectives on the bulk path.  Other combinations return
  * PL_ERR_UNSUPPORTED. */
 typedef enum { PL_SCHED_ITEM = 1, PL_SCHED_STREAM = 2, PL_SCHED_QUEUE = 3 } purlin_schedule;
 

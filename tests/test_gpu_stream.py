@@ -7,7 +7,9 @@ many items per CTA (small parts), small chunks and rings of 2..8 slots.
 Each case runs twice on one handle, the destinations cleared in between: the
 queue counter that the last CTA of a launch resets must start the second
 launch from zero.  A CUDA graph of queued calls replays several times, and
-the trace records every item exactly once.
+the trace records every item exactly once.  The queue on the register path
+runs every collective, the two-shot (SNAC) AllReduce included, whose
+dropped-notify time-out must leave the next calls correct.
 """
 
 import numpy as np
@@ -190,3 +192,132 @@ def test_stream_trace_records_every_item(schedule):
     want = oracle.all_to_all(ins)
     for r in range(world):
         assert np.array_equal(dst.read(r), want[r])
+
+
+# ------------------------------------------- the shared queue on the register path
+
+REGQ = {"path": P.PATH_REGISTER, "schedule": P.PL_SCHED_QUEUE}
+
+
+def draw(dtype, n):
+    x = RNG.standard_normal(n).astype(np.float32)
+    return x if dtype == "f32" else inputs.to_bf16_bits(x)
+
+
+@pytest.mark.parametrize("layout", [P.PL_LAYOUT_ONE_SHOT, P.PL_LAYOUT_TWO_SHOT])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("world", [2, 5, 8])
+def test_queued_all_reduce(layout, dtype, world):
+    E = 4 if dtype == "f32" else 2
+    n = 70001 * world + 3
+    ins = [draw(dtype, n) for _ in range(world)]
+    src = RankBuffers([n * E] * world, [0, 4, 8, 12, 0, 4, 8, 12][:world] if dtype == "f32" else None)
+    dst = RankBuffers([n * E] * world)
+    src.upload(ins)
+    h = Handle(world)
+    try:
+        P.check(P.purlin_tune_override(h.h, dict(REGQ, layout=layout, chunk_bytes=8192, interleave_bytes=16384)))
+        want = oracle.all_reduce(ins, dtype)
+        for _ in range(2):
+            dst.fill(0)
+            P.check(P.purlin_all_reduce(h.h, src.ptrs(), dst.ptrs(), n * E, P.PL_F32 if dtype == "f32" else P.PL_BF16,
+                                        0, stream()))
+            sync()
+            assert h.status() == 0
+            for r in range(world):
+                got = dst.read(r, np.float32 if dtype == "f32" else np.uint16)
+                assert np.array_equal(got.view(np.uint32) if dtype == "f32" else got,
+                                      want[r].view(np.uint32) if dtype == "f32" else want[r]), r
+        assert dst.guards_intact()
+    finally:
+        assert h.close() == P.PL_OK
+
+
+def test_queued_register_copies_and_reduce_scatter():
+    world = 8
+    tune = dict(REGQ, interleave_bytes=8192)
+    for S in (8 * 1000 + 8, 65536 + 48, (1 << 20) + 16 * 8):
+        ins = [RNG.integers(0, 256, size=S, dtype=np.uint8) for _ in range(world)]
+        expect(run_twice("ag", world, ins, S, [world * S] * world, tune, [1, 0, 3, 0, 5, 0, 7, 0]),
+               oracle.all_gather(ins))
+        expect(run_twice("a2a", world, ins, S, [S] * world, tune), oracle.all_to_all(ins))
+    C, c = inputs.w5_counts(world, max_count=30000, seed=4)
+    a2av_in, agv_in = inputs.w5_payloads(C, c, seed=4)
+    expect(run_twice("agv", world, agv_in, [int(v) * 2 for v in c], [int(c.sum()) * 2] * world, tune),
+           oracle.all_gather_v(agv_in, [int(v) for v in c]), np.uint16)
+    expect(run_twice("a2av", world, a2av_in, [int(v) * 2 for v in C.reshape(-1)],
+                     [int(C[:, d].sum()) * 2 for d in range(world)], tune), oracle.all_to_all_v(a2av_in, C), np.uint16)
+    n = 8 * 50001
+    ins = [draw("f32", n) for _ in range(world)]
+    src = RankBuffers([n * 4] * world)
+    dst = RankBuffers([n // world * 4] * world)
+    src.upload(ins)
+    h = Handle(world)
+    try:
+        P.check(P.purlin_tune_override(h.h, tune))
+        want = oracle.reduce_scatter(ins, "f32")
+        for _ in range(2):
+            dst.fill(0)
+            P.check(P.purlin_reduce_scatter(h.h, src.ptrs(), dst.ptrs(), n * 4, P.PL_F32, 0, stream()))
+            sync()
+            for r in range(world):
+                assert np.array_equal(dst.read(r, np.float32).view(np.uint32), want[r].view(np.uint32))
+    finally:
+        assert h.close() == P.PL_OK
+
+
+def test_queued_two_shot_wait_runs_out_and_recovers():
+    world, n = 4, 1 << 16
+    ins = [draw("f32", n) for _ in range(world)]
+    src = RankBuffers([n * 4] * world)
+    dst = RankBuffers([n * 4] * world)
+    src.upload(ins)
+    h = Handle(world)
+    try:
+        P.check(P.purlin_tune_override(h.h, dict(REGQ, layout=P.PL_LAYOUT_TWO_SHOT, chunk_bytes=4096)))
+        P.check(P.purlin_set_wait_timeout_ns(h.h, 20_000_000))
+        P.check(P.purlin_debug_drop_notify(h.h, 0))          # item 0 is a reduce that notifies
+        P.check(P.purlin_all_reduce(h.h, src.ptrs(), dst.ptrs(), n * 4, P.PL_F32, 0, stream()))
+        sync()
+        assert h.status() == P.PL_ERR_TIMEOUT
+        assert h.status() == 0
+        want = oracle.all_reduce(ins, "f32")
+        for _ in range(2):                                   # the queue counter starts from zero again
+            dst.fill(0)
+            P.check(P.purlin_all_reduce(h.h, src.ptrs(), dst.ptrs(), n * 4, P.PL_F32, 0, stream()))
+            sync()
+            assert h.status() == 0
+            for r in range(world):
+                assert np.array_equal(dst.read(r, np.float32).view(np.uint32), want[r].view(np.uint32))
+    finally:
+        assert h.close() == P.PL_OK
+
+
+def test_queued_two_shot_in_a_cuda_graph():
+    world, n = 8, (1 << 18) + 5
+    ins = [draw("bf16", n) for _ in range(world)]
+    src = RankBuffers([n * 2] * world)
+    dst = RankBuffers([n * 2] * world)
+    src.upload(ins)
+    h = Handle(world)
+    try:
+        P.check(P.purlin_tune_override(h.h, dict(REGQ, layout=P.PL_LAYOUT_TWO_SHOT, chunk_bytes=16384)))
+        s = torch.cuda.Stream()
+        want = oracle.all_reduce(ins, "bf16")
+        with torch.cuda.stream(s):
+            P.check(P.purlin_all_reduce(h.h, src.ptrs(), dst.ptrs(), n * 2, P.PL_BF16, 0, s.cuda_stream))
+            s.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(3):
+                    P.check(P.purlin_all_reduce(h.h, src.ptrs(), dst.ptrs(), n * 2, P.PL_BF16, 0, s.cuda_stream))
+            for _ in range(3):
+                dst.fill(0)
+                g.replay()
+                s.synchronize()
+                for r in range(world):
+                    assert np.array_equal(dst.read(r, np.uint16), want[r])
+            del g
+        assert h.status() == 0
+    finally:
+        assert h.close() == P.PL_OK

@@ -271,21 +271,44 @@ def test_queue_plans(part):
         assert np.array_equal(outs[r], want[r])
 
 
-def test_streamed_schedules_need_bulk_copies():
-    """Stream and queue schedules serve copy plans on the bulk path only."""
+def test_schedule_combinations():
+    """Stream: copy plans on the bulk path.  Queue: any plan on the register
+    path, copy plans on the bulk path."""
+    def st(coll, dtype, sizes, **tune):
+        return P.purlin_plan_describe(coll, 4, dtype, sizes, tune=tune)[0]
+    AG, RS, AR = P.PL_COLL_ALL_GATHER, P.PL_COLL_REDUCE_SCATTER, P.PL_COLL_ALL_REDUCE
     for sched in (P.PL_SCHED_STREAM, P.PL_SCHED_QUEUE):
-        st, *_ = P.purlin_plan_describe(P.PL_COLL_ALL_GATHER, 4, P.PL_U8, [1 << 20],
-                                        tune={"path": P.PATH_BULK, "schedule": sched})
-        assert st == P.PL_OK
-        st, *_ = P.purlin_plan_describe(P.PL_COLL_ALL_GATHER, 4, P.PL_U8, [1 << 20],
-                                        tune={"path": P.PATH_REGISTER, "schedule": sched})
-        assert st == P.PL_ERR_UNSUPPORTED
-        st, *_ = P.purlin_plan_describe(P.PL_COLL_REDUCE_SCATTER, 4, P.PL_F32, [1 << 20],
-                                        tune={"path": P.PATH_BULK, "schedule": sched})
-        assert st == P.PL_ERR_UNSUPPORTED
-        st, *_ = P.purlin_plan_describe(P.PL_COLL_ALL_REDUCE, 4, P.PL_F32, [1 << 20],
-                                        tune={"path": P.PATH_BULK, "schedule": sched,
-                                              "layout": P.PL_LAYOUT_TWO_SHOT})
-        assert st == P.PL_ERR_UNSUPPORTED
-    st, *_ = P.purlin_plan_describe(P.PL_COLL_ALL_GATHER, 4, P.PL_U8, [1 << 20], tune={"schedule": 4})
-    assert st == P.PL_ERR_INVALID_ARG
+        assert st(AG, P.PL_U8, [1 << 20], path=P.PATH_BULK, schedule=sched) == P.PL_OK
+        assert st(RS, P.PL_F32, [1 << 20], path=P.PATH_BULK, schedule=sched) == P.PL_ERR_UNSUPPORTED
+        assert st(AR, P.PL_F32, [1 << 20], path=P.PATH_BULK, schedule=sched,
+                  layout=P.PL_LAYOUT_TWO_SHOT) == P.PL_ERR_UNSUPPORTED
+    assert st(AG, P.PL_U8, [1 << 20], path=P.PATH_REGISTER, schedule=P.PL_SCHED_STREAM) == P.PL_ERR_UNSUPPORTED
+    for coll, dtype in ((AG, P.PL_U8), (RS, P.PL_F32), (AR, P.PL_BF16)):
+        assert st(coll, dtype, [1 << 20], path=P.PATH_REGISTER, schedule=P.PL_SCHED_QUEUE) == P.PL_OK
+    assert st(AR, P.PL_F32, [1 << 20], path=P.PATH_REGISTER, schedule=P.PL_SCHED_QUEUE,
+              layout=P.PL_LAYOUT_TWO_SHOT) == P.PL_OK
+    assert st(AG, P.PL_U8, [1 << 20], schedule=4) == P.PL_ERR_INVALID_ARG
+
+
+def test_queued_two_shot_plan_orders_every_wait_after_its_notify():
+    """The deadlock-freedom argument of the queue: waits point to earlier items."""
+    tune = {"path": P.PATH_REGISTER, "schedule": P.PL_SCHED_QUEUE, "layout": P.PL_LAYOUT_TWO_SHOT,
+            "chunk_bytes": 4096}
+    for world in (2, 3, 8):
+        n = 50000 * world + 7
+        st, items, grid, nflags = P.purlin_plan_describe(P.PL_COLL_ALL_REDUCE, world, P.PL_F32, [n * 4], None, None,
+                                                         152, tune)
+        assert st == P.PL_OK and nflags > 0
+        notified = {}
+        for i, it in enumerate(items):
+            assert it["cta"] == QUEUED and it["order"] == i
+            if it["wait"]:
+                assert notified.get(it["wait"], len(items)) < i
+            if it["notify"]:
+                notified[it["notify"]] = i
+        ins = [_draw("f32", n) for _ in range(world)]
+        outs = [np.zeros(n * 4, np.uint8) for _ in range(world)]
+        run_items(items, [_bytes(x) for x in ins], outs, "f32")
+        want = oracle.all_reduce(ins, "f32")
+        for r in range(world):
+            assert np.array_equal(outs[r], _bytes(want[r]))
