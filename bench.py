@@ -570,7 +570,11 @@ def side_table(P, h, stream, dev):
             f.ctx.dst[r] = dst[r].data_ptr()
         f.ctx.barrier = bar.data_ptr()
         f.bytes, f.out_bytes, f.which, f.work = nb_in, nb_out, which, 0
+        # the grid is the caller's choice: one CTA per SM for the AllGather
+        # (measured best), every resident CTA for the AllReduce
         g = EX.max_grid()
+        if which == EX.AG:
+            g = min(g, torch.cuda.get_device_properties(dev).multi_processor_count)
         f.coll_blocks = g
         f.status = status.data_ptr()
         times = timeit(lambda: EX.launch(f, g, stream.cuda_stream), graph=False)

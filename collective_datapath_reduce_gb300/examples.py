@@ -8,7 +8,7 @@ import ctypes
 from . import _build
 
 MAX_RANKS = 16
-AG, A2A, AR_BF16, RS_F32, AR_F32_8 = 0, 1, 2, 3, 4
+AG, A2A, AR_BF16, RS_F32, AR_F32_8, AG_STREAMING, AR_BF16_STREAMING, AR_BF16_U1 = 0, 1, 2, 3, 4, 5, 6, 7
 WORK_BEFORE, WORK_AFTER = 1, 2
 
 

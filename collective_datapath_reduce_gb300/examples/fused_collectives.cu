@@ -21,7 +21,9 @@ struct FusedArgs {
   unsigned char* post[purlin::kMaxRanks];      // results of the work after the call
   unsigned long long bytes;                    // per-rank input bytes
   unsigned long long out_bytes;                // per-rank output bytes
-  int which;                                   // 0 AG, 1 A2A, 2 AR bf16, 3 RS fp32, 4 AR fp32 world 8
+  int which;                                   // 0 AG, 1 A2A, 2 AR bf16, 3 RS fp32, 4 AR fp32 world 8;
+                                               // 5 AG and 6 AR bf16 with evict-first stores,
+                                               // 7 AR bf16 with one vector per source in flight
   int coll_blocks;
   int* status;
   int work;                                    // bit 0: work before the call, bit 1: work after
@@ -37,7 +39,8 @@ __global__ void __launch_bounds__(256) fused_kernel(const __grid_constant__ Fuse
       const int r = (int)(k / f.bytes);
       const unsigned long long i = k % f.bytes;
       const unsigned char x = f.in[r][i];
-      const_cast<char*>(f.ctx.src[r])[i] = (char)(f.which <= 1 ? (x ^ 0x5A) : x);
+      const bool copy = f.which <= 1 || f.which == 5;
+      const_cast<char*>(f.ctx.src[r])[i] = (char)(copy ? (x ^ 0x5A) : x);
     }
   }
   const purlin::SnacArgs a{f.bytes, (int)gridDim.x, f.coll_blocks, (int)blockIdx.x, (f.work & 2) != 0};
@@ -49,6 +52,14 @@ __global__ void __launch_bounds__(256) fused_kernel(const __grid_constant__ Fuse
       st = N == 8 ? purlin::all_reduce<pl::bf16_tag, 8>(a, f.ctx) : purlin::all_reduce<pl::bf16_tag>(a, f.ctx);
       break;
     case 3: st = purlin::reduce_scatter<float>(a, f.ctx); break;
+    case 5: st = purlin::all_gather<true>(a, f.ctx); break;
+    case 6:
+      st = N == 8 ? purlin::all_reduce<pl::bf16_tag, 8, 2, true>(a, f.ctx)
+                  : purlin::all_reduce<pl::bf16_tag, 0, 2, true>(a, f.ctx);
+      break;
+    case 7:  // one vector per source in flight (the smallest register footprint)
+      st = N == 8 ? purlin::all_reduce<pl::bf16_tag, 8, 1>(a, f.ctx) : purlin::all_reduce<pl::bf16_tag, 0, 1>(a, f.ctx);
+      break;
     default: st = purlin::all_reduce<float, 8>(a, f.ctx); break;
   }
   if (threadIdx.x == 0 && st != purlin::kOk) atomicExch(f.status, st);

@@ -111,7 +111,7 @@ struct Piece {
 // This CTA's share of the concatenated pieces (part `part` of `nparts`, cut at
 // 512-byte granules of each piece), and the Atom on every overlapped piece.
 // `piece(i)` returns piece i; pieces are produced on the fly (no arrays).
-template <typename T, int NS, class PieceFn>
+template <typename T, int NS, int U, bool STREAMING, class PieceFn>
 __device__ void run_share(const Context& c, PieceFn piece, int npieces, int part, int nparts) {
   __shared__ const char* s_src[kMaxRanks];
   __shared__ char* s_dst[kMaxRanks];
@@ -150,16 +150,16 @@ __device__ void run_share(const Context& c, PieceFn piece, int npieces, int part
     // the sources were written earlier in this launch: coherent (L2) loads
     if (ns == 1) {
       if (same) {
-        pl::copy_atom<true, 2, false>(s_src[0], s_dst, nd, e - a);
+        pl::copy_atom<true, 2, STREAMING>(s_src[0], s_dst, nd, e - a);
       } else {
-        for (int j = 0; j < nd; ++j) pl::copy_atom<true, 2, false>(s_src[0], s_dst + j, 1, e - a);
+        for (int j = 0; j < nd; ++j) pl::copy_atom<true, 2, STREAMING>(s_src[0], s_dst + j, 1, e - a);
       }
     } else {
       if constexpr (!std::is_same<T, void>::value) {
         if (same) {
-          pl::reduce_atom<T, NS, 1, false, true>(s_src, ns, s_dst, nd, e - a);
+          pl::reduce_atom<T, NS, U, STREAMING, true>(s_src, ns, s_dst, nd, e - a);
         } else {
-          for (int j = 0; j < nd; ++j) pl::reduce_atom<T, NS, 1, false, true>(s_src, ns, s_dst + j, 1, e - a);
+          for (int j = 0; j < nd; ++j) pl::reduce_atom<T, NS, U, STREAMING, true>(s_src, ns, s_dst + j, 1, e - a);
         }
       }
     }
@@ -167,10 +167,10 @@ __device__ void run_share(const Context& c, PieceFn piece, int npieces, int part
   __syncthreads();
 }
 
-template <typename T, int NS, class PieceFn>
+template <typename T, int NS, int U, bool STREAMING, class PieceFn>
 __device__ int collective(const SnacArgs& a, const Context& c, PieceFn piece, int npieces) {
   if (grid_barrier(c, a.blocks) != kOk) return kTimeout;
-  if (a.b_idx < a.coll_blocks) run_share<T, NS>(c, piece, npieces, a.b_idx, a.coll_blocks);
+  if (a.b_idx < a.coll_blocks) run_share<T, NS, U, STREAMING>(c, piece, npieces, a.b_idx, a.coll_blocks);
   if (a.sync_after && grid_barrier(c, a.blocks) != kOk) return kTimeout;
   return kOk;
 }
@@ -180,15 +180,19 @@ __device__ __forceinline__ unsigned all_ranks(int world) { return world >= 32 ? 
 }  // namespace detail
 
 // AllGather (NKI all_gather_hbm_kernel): dst[r] = src[0] || ... || src[N-1].
+// STREAMING (every collective below takes it too): evict-first stores, which
+// keep the stored lines from displacing the sources in the L2.
+template <bool STREAMING = false>
 __device__ inline int all_gather(const SnacArgs& a, const Context& c) {
   const unsigned long long S = a.bytes;
   const unsigned all = detail::all_ranks(c.world);
   auto piece = [=](int s) { return detail::Piece{0ull, s * S, S, 1u << s, all}; };
-  return detail::collective<void, 1>(a, c, piece, c.world);
+  return detail::collective<void, 1, 1, STREAMING>(a, c, piece, c.world);
 }
 
 // AllToAll (NKI all_to_all_hbm_kernel): chunk d of src[s] -> chunk s of dst[d];
 // bytes must split into world chunks.
+template <bool STREAMING = false>
 __device__ inline int all_to_all(const SnacArgs& a, const Context& c) {
   const int N = c.world;
   const unsigned long long ch = a.bytes / (unsigned)N;
@@ -196,27 +200,28 @@ __device__ inline int all_to_all(const SnacArgs& a, const Context& c) {
     const int s = i / N, d = i % N;
     return detail::Piece{d * ch, s * ch, ch, 1u << s, 1u << d};
   };
-  return detail::collective<void, 1>(a, c, piece, N * N);
+  return detail::collective<void, 1, 1, STREAMING>(a, c, piece, N * N);
 }
 
 // AllReduce (NKI all_reduce_hbm_kernel), one-shot layout: T = float or
-// pl::bf16_tag; NS = world if known at compile time (2..8), else 0.
-template <typename T, int NS = 0>
+// pl::bf16_tag; NS = world if known at compile time (2..8), else 0; U =
+// 16-byte vectors each thread keeps in flight per source.
+template <typename T, int NS = 0, int U = 2, bool STREAMING = false>
 __device__ int all_reduce(const SnacArgs& a, const Context& c) {
   const unsigned all = detail::all_ranks(c.world);
   const unsigned long long S = a.bytes;
   auto piece = [=](int) { return detail::Piece{0ull, 0ull, S, all, all}; };
-  return detail::collective<T, NS>(a, c, piece, 1);
+  return detail::collective<T, NS, U, STREAMING>(a, c, piece, 1);
 }
 
 // ReduceScatter (NKI reduce_scatter_hbm_kernel): dst[r] = chunk r of the sum;
 // bytes (per-rank input) must split into world chunks of whole elements.
-template <typename T, int NS = 0>
+template <typename T, int NS = 0, int U = 2, bool STREAMING = false>
 __device__ int reduce_scatter(const SnacArgs& a, const Context& c) {
   const unsigned long long ch = a.bytes / (unsigned)c.world;
   const unsigned all = detail::all_ranks(c.world);
   auto piece = [=](int r) { return detail::Piece{r * ch, 0ull, ch, all, 1u << r}; };
-  return detail::collective<T, NS>(a, c, piece, c.world);
+  return detail::collective<T, NS, U, STREAMING>(a, c, piece, c.world);
 }
 
 }  // namespace purlin

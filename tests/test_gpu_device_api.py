@@ -75,6 +75,25 @@ def test_fused_all_gather_and_all_to_all(lib, coll_frac):
         assert np.array_equal(outs[r], want[r])
 
 
+def test_fused_streaming_store_variants(lib):
+    """The evict-first store forms, and one vector per source in flight, give the same bytes."""
+    rng = np.random.default_rng(33)
+    world, S = 8, (1 << 19) + 48
+    ins = [rng.integers(0, 256, size=S, dtype=np.uint8) for _ in range(world)]
+    outs = run(lib, EX.AG_STREAMING, world, ins, world * S)
+    want = oracle.all_gather([x ^ 0x5A for x in ins])
+    for r in range(world):
+        assert np.array_equal(outs[r], want[r])
+    for world in (8, 5):
+        n = 200003
+        ins = [inputs.to_bf16_bits(rng.standard_normal(n).astype(np.float32)) for _ in range(world)]
+        want = oracle.all_reduce(ins, "bf16")
+        for which in (EX.AR_BF16_STREAMING, EX.AR_BF16_U1):
+            outs = run(lib, which, world, ins, n * 2)
+            for r in range(world):
+                assert np.array_equal(outs[r].view(np.uint16), want[r])
+
+
 def test_fused_reductions(lib):
     rng = np.random.default_rng(32)
     world, n = 5, 300001
