@@ -22,6 +22,8 @@ BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIBNAME = "libpurlin_gb.so"
 LIBPATH = os.path.join(LIBDIR, LIBNAME)
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIBPATH_DEBUG = os.path.join(LIBDIR, "libpurlin_gb_debug.so")
 EXAMPLES = os.path.join(PKG, "examples")
 EXAMPLES_PATH = os.path.join(LIBDIR, "libpurlin_examples.so")
 
@@ -75,9 +77,15 @@ def build_examples(verbose: bool = False, force: bool = False) -> str:
     return EXAMPLES_PATH
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
-    """Compile (if needed) and return the path of libpurlin_gb.so (and the examples library)."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, debug: bool = False) -> str:
+    """Compile (if needed) and return the path of libpurlin_gb.so (and the examples library).
+
+    debug=True builds the checking library libpurlin_gb_debug.so instead
+    (PURLIN_DEBUG: every kernel checks each work item against the rank
+    buffers' sizes before it moves data)."""
+    bdir = BUILD_DEBUG if debug else BUILD
+    libpath = LIBPATH_DEBUG if debug else LIBPATH
+    os.makedirs(bdir, exist_ok=True)
     os.makedirs(LIBDIR, exist_ok=True)
     srcs = _sources()
     hdr_time = _newest(_headers())
@@ -85,10 +93,10 @@ def build(verbose: bool = False, force: bool = False) -> str:
     jobs = []
     objs = []
     for src in srcs:
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
         objs.append(obj)
         if force or not os.path.exists(obj) or os.path.getmtime(obj) < max(os.path.getmtime(src), hdr_time):
-            cmd = [cc, *ARCH, *CFLAGS, "-c", src, "-o", obj]
+            cmd = [cc, *ARCH, *CFLAGS, *(["-DPURLIN_DEBUG"] if debug else []), "-c", src, "-o", obj]
             if src.endswith(".cu") and verbose:
                 cmd.insert(1, "-Xptxas=-v")
             jobs.append(cmd)
@@ -104,15 +112,16 @@ def build(verbose: bool = False, force: bool = False) -> str:
                     print(r.stdout + r.stderr)
                 if r.returncode != 0:
                     raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
-    if jobs or not os.path.exists(LIBPATH) or os.path.getmtime(LIBPATH) < _newest(objs):
-        tmp = LIBPATH + ".tmp"
+    if jobs or not os.path.exists(libpath) or os.path.getmtime(libpath) < _newest(objs):
+        tmp = libpath + ".tmp"
         cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-Xcompiler", "-fPIC"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
-        os.replace(tmp, LIBPATH)
-    build_examples(verbose, force)
-    return LIBPATH
+        os.replace(tmp, libpath)
+    if not debug:
+        build_examples(verbose, force)
+    return libpath
 
 
 if __name__ == "__main__":

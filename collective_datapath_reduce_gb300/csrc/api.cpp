@@ -61,6 +61,8 @@ struct purlin_ctx {
   bool has_over = false;
   unsigned long long timeout_ns = kDefaultTimeoutNs;
   long long drop_notify = -1;
+  int limit_side = -1, limit_rank = 0;  // purlin_debug_limit_buffer, for the next launch
+  uint64_t limit_bytes = 0;
   unsigned long long* trace = nullptr;  // caller's trace buffer, or nullptr
   uint32_t trace_cap = 0;
   bool finalized = false;
@@ -357,6 +359,15 @@ purlin_status run(purlin_ctx* h, int coll, int world, int dtype, const uint64_t*
   a.trace = h->trace;
   a.trace_cap = h->trace_cap;
   h->drop_notify = -1;
+  for (int r = 0; r < pl::kMaxWorld; ++r) {
+    a.in_bytes[r] = d->plan.in_bytes[r];
+    a.out_bytes[r] = d->plan.out_bytes[r];
+  }
+  if (h->limit_side >= 0) {
+    uint64_t* b = h->limit_side ? a.out_bytes : a.in_bytes;
+    b[h->limit_rank] = std::min<uint64_t>(b[h->limit_rank], h->limit_bytes);
+    h->limit_side = -1;
+  }
 
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
@@ -705,6 +716,7 @@ const char* purlin_status_string(purlin_status s) {
     case PL_ERR_LAUNCH: return "kernel launch failed";
     case PL_ERR_TIMEOUT: return "a SNAC wait on the device ran out of time";
     case PL_ERR_FINALIZED: return "handle already finalized";
+    case PL_ERR_BOUNDS: return "a work item reached outside a rank buffer (checking build)";
   }
   return "unknown status";
 }
@@ -747,6 +759,17 @@ purlin_status purlin_debug_drop_notify(purlin_handle h, long long item) {
   purlin_status st;
   if ((st = check_handle(h))) return st;
   h->drop_notify = item < 0 ? -1 : item;
+  return PL_OK;
+}
+
+purlin_status purlin_debug_limit_buffer(purlin_handle h, int is_output, int rank, uint64_t bytes) {
+  purlin_status st;
+  if ((st = check_handle(h))) return st;
+  if (rank < 0 || rank >= PURLIN_MAX_WORLD) return PL_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(h->mu);
+  h->limit_side = is_output ? 1 : 0;
+  h->limit_rank = rank;
+  h->limit_bytes = bytes;
   return PL_OK;
 }
 

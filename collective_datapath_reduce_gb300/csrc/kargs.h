@@ -14,6 +14,7 @@ namespace pl {
 enum : int { kCtlStatus = 0, kCtlEpoch = 1, kCtlDone = 2, kCtlQueue = 3, kCtlQueueDone = 4 };
 constexpr int kCtlBytes = 256;   // flags start here
 constexpr int kDevTimeout = 7;   // PL_ERR_TIMEOUT
+constexpr int kDevBounds = 9;    // PL_ERR_BOUNDS (checking build)
 
 struct KArgs {
   const char* in[kMaxWorld];
@@ -34,6 +35,8 @@ struct KArgs {
   uint32_t chunk_bytes;       // bulk path: bytes per source tile in a slot
   unsigned long long* trace;  // trace buffer (header word + records), or nullptr
   uint32_t trace_cap;         // records the trace buffer holds
+  uint64_t in_bytes[kMaxWorld];   // bytes of each input and output buffer (the
+  uint64_t out_bytes[kMaxWorld];  // checking build tests every item against them)
 };
 
 // One trace record (32 bytes): which CTA ran which item, when, and how long it

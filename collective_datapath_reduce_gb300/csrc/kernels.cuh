@@ -63,6 +63,27 @@ __device__ __forceinline__ bool consume_wait(const KArgs& a, const uint32_t* fla
 // GB300 that gained nothing over this.
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Checking build (PURLIN_DEBUG): true when every byte item `it` reads and
+// writes lies inside the rank buffers' declared sizes.  The normal build
+// does not check.
+__device__ __forceinline__ bool item_in_bounds(const KArgs& a, const Item& it) {
+#ifdef PURLIN_DEBUG
+  const uint64_t end = it.src_off + it.len;
+  if (end < it.src_off || it.dst_off + it.len < it.dst_off) return false;
+  for (uint32_t m = it.src_mask; m; m &= m - 1) {
+    const int b = __ffs(m) - 1;
+    if (end > (b < 16 ? a.in_bytes[b] : a.out_bytes[b - 16])) return false;
+  }
+  for (uint32_t m = it.dst_mask; m; m &= m - 1)
+    if (it.dst_off + it.len > a.out_bytes[__ffs(m) - 1]) return false;
+  return true;
+#else
+  (void)a;
+  (void)it;
+  return true;
+#endif
+}
+
 // Append one record to the trace buffer (thread 0).  Records past the
 // capacity are counted but not written.
 __device__ __forceinline__ void trace_put(const KArgs& a, unsigned long long t0, unsigned long long t1,
@@ -163,6 +184,10 @@ __global__ void __launch_bounds__(512, 2) snac_kernel(const __grid_constant__ KA
         s_ns = ns;
         s_nd = nd;
         s_len = it.len;
+        if (!item_in_bounds(a, it)) {  // checking build: move nothing, keep the SNAC order
+          atomicCAS(&a.ctl[kCtlStatus], 0u, (uint32_t)kDevBounds);
+          s_len = 0;
+        }
         s_notify = it.notify;
         int ok = 1;
         const unsigned long long t0 = a.trace ? globaltimer() : 0ull;

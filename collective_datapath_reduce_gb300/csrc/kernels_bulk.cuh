@@ -378,6 +378,10 @@ __global__ void __launch_bounds__(512, 1) bulk_kernel(const __grid_constant__ KA
       s_ns = ns;
       s_nd = nd;
       s_len = it.len;
+      if (!item_in_bounds(a, it)) {  // checking build: move nothing, keep the SNAC order
+        atomicCAS(&a.ctl[kCtlStatus], 0u, (uint32_t)kDevBounds);
+        s_len = 0;
+      }
       s_notify = it.notify;
       s_aligned = (orr & 15u) == 0;
       int ok = 1;

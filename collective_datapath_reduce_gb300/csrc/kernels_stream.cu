@@ -115,9 +115,13 @@ __global__ void __launch_bounds__(512, 1) stream_copy_kernel(const __grid_consta
         ++issued;
         return;
       }
-      const Item it = nx;
+      Item it = nx;
       const uint32_t idx = nx_idx;
       advance();
+      if (!item_in_bounds(a, it)) {  // checking build: move nothing
+        atomicCAS(&a.ctl[kCtlStatus], 0u, (uint32_t)kDevBounds);
+        it.len = 0;
+      }
       StreamItem& u = SI[p_item % kItemRing];
       p_cur = p_item % kItemRing;
       ++p_item;

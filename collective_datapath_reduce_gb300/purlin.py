@@ -25,6 +25,7 @@ PL_ERR_CUDA = 5
 PL_ERR_LAUNCH = 6
 PL_ERR_TIMEOUT = 7
 PL_ERR_FINALIZED = 8
+PL_ERR_BOUNDS = 9
 
 PL_U8, PL_F32, PL_BF16 = 0, 1, 2
 PL_DETERMINISTIC = 0
@@ -91,6 +92,7 @@ _SIGNATURES = {
     "purlin_tune_get": (_i, [_vp, _i, _i, _sz, ctypes.POINTER(purlin_tune)]),
     "purlin_tune_override": (_i, [_vp, ctypes.POINTER(purlin_tune)]),
     "purlin_set_wait_timeout_ns": (_i, [_vp, ctypes.c_uint64]),
+    "purlin_debug_limit_buffer": (_i, [_vp, _i, _i, ctypes.c_uint64]),
     "purlin_debug_drop_notify": (_i, [_vp, ctypes.c_longlong]),
     "purlin_query": (_i, [_vp, ctypes.POINTER(_i), ctypes.POINTER(_i), ctypes.POINTER(_i)]),
     "purlin_all_reduce_noalloc": (_i, [_i, _PP, _PP, _sz, _i, _vp, _vp]),
@@ -121,6 +123,35 @@ def load():
             fn.argtypes = args
         _lib = lib
     return _lib
+
+
+def load_checking():
+    """Build (if needed) and load the checking library libpurlin_gb_debug.so
+    (work items checked against buffer sizes on the device).  Returns the
+    library; `using(lib)` makes the wrappers of this module call it."""
+    path = _build.build(debug=True)
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+class using:
+    """Context manager: the wrappers call `lib` (a loaded library) inside."""
+
+    def __init__(self, lib):
+        self.lib = lib
+
+    def __enter__(self):
+        global _lib
+        self.prev, _lib = load(), self.lib
+        return self.lib
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self.prev
 
 
 def declared_symbols() -> list[str]:
@@ -266,6 +297,10 @@ def purlin_set_wait_timeout_ns(h, ns: int) -> int:
 
 def purlin_debug_drop_notify(h, item: int) -> int:
     return load().purlin_debug_drop_notify(h, item)
+
+
+def purlin_debug_limit_buffer(h, is_output: int, rank: int, nbytes: int) -> int:
+    return load().purlin_debug_limit_buffer(h, int(is_output), int(rank), int(nbytes))
 
 
 def purlin_trace_enable(h, buffer=None, buffer_bytes: int = 0) -> int:

@@ -69,7 +69,8 @@ typedef enum {
   PL_ERR_CUDA = 5,         /* a CUDA runtime call failed */
   PL_ERR_LAUNCH = 6,       /* the kernel could not be launched */
   PL_ERR_TIMEOUT = 7,      /* device: a SNAC consume wait gave up */
-  PL_ERR_FINALIZED = 8     /* the handle was finalized */
+  PL_ERR_FINALIZED = 8,    /* the handle was finalized */
+  PL_ERR_BOUNDS = 9        /* device, checking build only: a work item reached outside a rank buffer */
 } purlin_status;
 
 typedef enum { PL_U8 = 0, PL_F32 = 1, PL_BF16 = 2 } purlin_dtype;
@@ -252,6 +253,17 @@ purlin_status purlin_tune_get(purlin_handle h, purlin_coll coll, purlin_dtype dt
 /* Override the tuning table for every later call on the handle (non-zero
  * fields win); NULL restores the table.  Used by the tuning sweep. */
 purlin_status purlin_tune_override(purlin_handle h, const purlin_tune* t);
+
+/* Test hook of the checking build (libpurlin_gb_debug.so, compiled with
+ * PURLIN_DEBUG): every kernel checks each work item against the byte count
+ * of every rank buffer it touches before it moves any data; an item that
+ * would reach outside is skipped (its SNAC notify still raised) and the
+ * device status reads PL_ERR_BOUNDS.  This hook makes the next launch on the
+ * handle believe that buffer `rank` (an input if is_output is 0, else an
+ * output) holds only `bytes` bytes, so a test can see the check fire without
+ * any access outside a buffer.  In the normal build the call is accepted and
+ * has no effect (there is no check to fire). */
+purlin_status purlin_debug_limit_buffer(purlin_handle h, int is_output, int rank, uint64_t bytes);
 
 /* Time limit of every SNAC consume wait, in nanoseconds (default 2e9). */
 purlin_status purlin_set_wait_timeout_ns(purlin_handle h, uint64_t ns);
