@@ -360,8 +360,10 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
         for (int o = 0; o < world; ++o) n_items += 2 * tiles[o];
         const uint64_t gcap = (uint64_t)p.tune.ctas_per_sm * sm_count;
         const uint64_t G = std::max<uint64_t>(1, std::min<uint64_t>(gcap, n_items));
-        // a copy round trails its reduce round by about one wave of CTAs
-        const uint64_t lag = std::max<uint64_t>(1, ceil_div(G, 2ull * world));
+        // a copy round trails its reduce round by about two waves of CTAs, so
+        // the reduce has usually finished when its copies start (one wave:
+        // 63.8 / 193.9 us at 8 x 16 / 64 MiB; two: 53.4 / 186.0 us)
+        const uint64_t lag = std::max<uint64_t>(1, ceil_div(G, (uint64_t)world));
         auto reduce_piece = [&](int o, uint64_t t) {
           uint64_t off = start[o] + t * T, len = std::min(T, start[o + 1] - off);
           Piece q{off, off, len, ALL, 1u << o, 0, (uint32_t)(o * tmax + t + 1)};
