@@ -106,12 +106,14 @@ size_t n_sizes(int coll, int world) {
 //               MiB; one CTA per SM or more gave 90-92%: fewer concurrent DRAM
 //               streams win); the fewest bytes per CTA stay at 512 so small
 //               calls spread over many CTAs.
-//   ReduceScatter  from 8 MiB per rank the TMA bulk ring (2 slots x 32 KiB
-//               per source) runs above the copy bandwidth: the traffic is
-//               8 reads per write.  Below that, the register path.
-//   AllGather   from 16 MiB per rank the streamed bulk ring fed from the
+//   ReduceScatter  the register path, 3 CTAs of 256 threads per SM, evict-
+//               first stores: above the copy bandwidth from 128 MiB per rank
+//               (the traffic is 8 reads per write); the TMA bulk ring
+//               (2 slots x 32 KiB per source) matches it from 64 MiB and
+//               trails it by 10% at 16-32 MiB.
+//   AllGather   from 8 MiB per rank the streamed bulk ring fed from the
 //               shared item queue in 16 KiB parts (6904 against 6466 GB/s for
-//               register copies at 8 x 256 MiB, 6529 against 6254 at 16 MiB);
+//               register copies at 8 x 256 MiB, 6361 against 5572 at 8 MiB);
 //               from 4 MiB register copies on 128 CTAs of 512 threads with
 //               evict-first stores (5756 against 5646 at 4 MiB).  AllGatherV
 //               (misaligned pieces): the queue in 32 KiB parts on 128 CTAs
@@ -154,16 +156,12 @@ Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
       break;
     case kReduceScatter:
     case kReduceScatterV:
+      // register path, three CTAs per SM, evict-first stores at every size
+      // (against the bulk ring: 6216 / 5567 GB/s at 8 x 16 MiB fp32, 6750 /
+      // 6163 at 32 MiB, even from 64 MiB up)
       t.unroll = world <= 4 ? 2 : 1;
-      if (S >= 8 * MiB) {
-        t.path = kPathBulk;
-        t.ctas_per_sm = 1;
-        t.stages = 2;
-        t.chunk_bytes = 32 * 1024;
-      } else {
-        t.ctas_per_sm = 3;
-        t.store_hint = 2;
-      }
+      t.ctas_per_sm = 3;
+      t.store_hint = 2;
       break;
     case kAllGather:
     case kAllGatherV:
@@ -193,7 +191,7 @@ Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
         t.chunk_bytes = 32 * 1024;
         t.schedule = kSchedQueue;
         t.interleave_bytes = 32 * 1024;
-      } else if (S >= 16 * MiB && coll == kAllGather) {
+      } else if (S >= 8 * MiB && coll == kAllGather) {
         // one bulk load, eight bulk stores per chunk; 16 KiB parts from the
         // shared queue, one CTA per SM
         t.path = kPathBulk;
