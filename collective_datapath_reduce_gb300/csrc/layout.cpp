@@ -106,11 +106,11 @@ size_t n_sizes(int coll, int world) {
 //               MiB; one CTA per SM or more gave 90-92%: fewer concurrent DRAM
 //               streams win); the fewest bytes per CTA stay at 512 so small
 //               calls spread over many CTAs.
-//   ReduceScatter  the register path, 3 CTAs of 256 threads per SM, evict-
-//               first stores: above the copy bandwidth from 128 MiB per rank
-//               (the traffic is 8 reads per write); the TMA bulk ring
-//               (2 slots x 32 KiB per source) matches it from 64 MiB and
-//               trails it by 10% at 16-32 MiB.
+//   ReduceScatter  from 64 MiB per rank the TMA bulk ring (2 slots x 32 KiB
+//               per source), above the copy bandwidth from 128 MiB (the
+//               traffic is 8 reads per write); below, the register path with
+//               3 CTAs of 256 threads per SM and evict-first stores (10%
+//               ahead of the ring at 16-32 MiB).
 //   AllGather   from 8 MiB per rank the streamed bulk ring fed from the
 //               shared item queue in 16 KiB parts (6904 against 6466 GB/s for
 //               register copies at 8 x 256 MiB, 6361 against 5572 at 8 MiB);
@@ -156,12 +156,21 @@ Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
       break;
     case kReduceScatter:
     case kReduceScatterV:
-      // register path, three CTAs per SM, evict-first stores at every size
-      // (against the bulk ring: 6216 / 5567 GB/s at 8 x 16 MiB fp32, 6750 /
-      // 6163 at 32 MiB, even from 64 MiB up)
       t.unroll = world <= 4 ? 2 : 1;
-      t.ctas_per_sm = 3;
-      t.store_hint = 2;
+      if (S >= 64 * MiB) {
+        // the bulk ring: level with the register path when calls run back to
+        // back, and unaffected by what the L2 held before the call (after an
+        // L2-sized write the register path loses 7% at 8 x 256 MiB fp32)
+        t.path = kPathBulk;
+        t.ctas_per_sm = 1;
+        t.stages = 2;
+        t.chunk_bytes = 32 * 1024;
+      } else {
+        // register path, three CTAs per SM, evict-first stores (against the
+        // bulk ring: 6216 / 5567 GB/s at 8 x 16 MiB fp32, 6750 / 6163 at 32 MiB)
+        t.ctas_per_sm = 3;
+        t.store_hint = 2;
+      }
       break;
     case kAllGather:
     case kAllGatherV:
