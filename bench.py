@@ -445,7 +445,9 @@ def side_table(P, h, stream, dev):
     a write of twice the L2 size; the point gives the median and the 10th /
     90th percentiles of the time per call.  Points whose working set fits in
     the L2 are marked: after the first call of a replay they run from the L2.
-    The copy reference is 10 plain launches of torch's copy kernel."""
+    Collective points also give the pages' own figure, totalBytes over time
+    (input bytes per rank; the output size for AllGather).  The copy
+    reference is 10 plain launches of torch's copy kernel."""
     import torch
     gen = torch.Generator(device=dev)
     gen.manual_seed(7)
@@ -493,13 +495,17 @@ def side_table(P, h, stream, dev):
                     for _ in range(count)]
         return [torch.randn(max(n, 1), dtype=dtype, device=dev, generator=gen) for _ in range(count)]
 
-    def point(nbytes, times):
-        # the algorithmic bytes are the distinct bytes a call touches: its working set
+    def point(nbytes, times, total_bytes=None):
+        # the algorithmic bytes are the distinct bytes a call touches: its working set.
+        # total_bytes: the pages' own bandwidth convention (purlin bench: input bytes
+        # per rank, the output size for AllGather), reported beside it for context.
         t = sorted(times)
         med = statistics.median(t)
         pct = lambda q: t[min(len(t) - 1, int(q * (len(t) - 1) + 0.5))]
         d = {"bytes": nbytes, "us": round(med * 1e3, 2), "us_p10": round(pct(0.1) * 1e3, 2),
              "us_p90": round(pct(0.9) * 1e3, 2), "GB/s": round(nbytes / (med / 1e3) / 1e9, 1)}
+        if total_bytes is not None:
+            d["totalBytes_GB/s"] = round(total_bytes / (med / 1e3) / 1e9, 1)
         if nbytes <= l2:
             d["l2_resident"] = True
         return d
@@ -513,11 +519,12 @@ def side_table(P, h, stream, dev):
         src = bufs(size, WORLD)
         dag = [torch.empty(WORLD * size, dtype=torch.uint8, device=dev) for _ in range(WORLD)]
         out["all_gather_u8"][key] = point(WORLD * size * (1 + WORLD),
-                                          timeit(lambda: chk(P.purlin_all_gather(h, src, dag, size, stream))))
+                                          timeit(lambda: chk(P.purlin_all_gather(h, src, dag, size, stream))),
+                                          WORLD * size)
         del dag
         da = [torch.empty(size, dtype=torch.uint8, device=dev) for _ in range(WORLD)]
         out["all_to_all_u8"][key] = point(2 * WORLD * size,
-                                          timeit(lambda: chk(P.purlin_all_to_all(h, src, da, size, stream))))
+                                          timeit(lambda: chk(P.purlin_all_to_all(h, src, da, size, stream))), size)
         big = torch.empty(2 * WORLD * size, dtype=torch.uint8, device=dev)
         half = WORLD * size
         # the copy kernel torch launches outside a graph (inside one, copy_ becomes
@@ -530,17 +537,17 @@ def side_table(P, h, stream, dev):
         x = bufs(size // 2, WORLD, torch.bfloat16)
         y = [torch.empty_like(t) for t in x]
         out["all_reduce_bf16"][key] = point(2 * WORLD * size, timeit(
-            lambda: chk(P.purlin_all_reduce(h, x, y, size, P.PL_BF16, 0, stream))))
+            lambda: chk(P.purlin_all_reduce(h, x, y, size, P.PL_BF16, 0, stream))), size)
         if size >= 16 * MI:
             P.check(P.purlin_tune_override(h, {"layout": P.PL_LAYOUT_TWO_SHOT}))
             out["all_reduce_two_shot_bf16"][key] = point(2 * WORLD * size, timeit(
-                lambda: chk(P.purlin_all_reduce(h, x, y, size, P.PL_BF16, 0, stream))))
+                lambda: chk(P.purlin_all_reduce(h, x, y, size, P.PL_BF16, 0, stream))), size)
             P.check(P.purlin_tune_override(h, None))
         del x, y
         x = bufs(size // 4, WORLD, torch.float32)
         y = [torch.empty(size // 4 // WORLD, dtype=torch.float32, device=dev) for _ in range(WORLD)]
         out["reduce_scatter_f32"][key] = point(WORLD * size + size, timeit(
-            lambda: chk(P.purlin_reduce_scatter(h, x, y, size, P.PL_F32, 0, stream))))
+            lambda: chk(P.purlin_reduce_scatter(h, x, y, size, P.PL_F32, 0, stream))), size)
         del x, y
         torch.cuda.empty_cache()
     # ReduceScatterV: uneven chunks (workload 5's first row of counts), bf16
