@@ -123,8 +123,15 @@ __device__ __forceinline__ void run_item(const char* const* src, int ns, char* c
 // its prefetch registers) an index larger than the one it runs, so the
 // earliest unfinished item is always running and the queue cannot deadlock
 // a SNAC plan (all CTAs are resident: cooperative launch).
+// Launch bound of the register-path kernel: 512 threads for the source
+// counts known at compile time; the generic count (up to 16 sources, in
+// batches of 8) runs 256-thread CTAs with room for 128 registers, so its 16
+// source pointers and 8 vectors in flight stay in registers.
+template <int NS>
+constexpr int snac_max_threads() { return NS == 0 ? 256 : 512; }
+
 template <typename T, int NS, int U>
-__global__ void __launch_bounds__(512, 2) snac_kernel(const __grid_constant__ KArgs a) {
+__global__ void __launch_bounds__(snac_max_threads<NS>(), 2) snac_kernel(const __grid_constant__ KArgs a) {
   constexpr uint32_t kNoItem = 0xFFFFFFFFu;
   __shared__ const char* s_src[kMaxWorld];
   __shared__ char* s_dst[kMaxWorld];

@@ -100,12 +100,13 @@ size_t n_sizes(int coll, int world) {
 // Tuning table, from the sweeps measured on a GB300 (152 SMs, HBM3e):
 // `bytes_per_rank` is the per-rank size the collective moves (for the V
 // variants, their total divided by the world).  Summary of what won:
-//   AllReduce   register path, 512 threads; from 8 MiB per rank 128 CTAs with
+//   AllReduce   (8 ranks) register path, 512 threads; from 8 MiB per rank 128 CTAs with
 //               one contiguous share each and evict-first stores (96% of the
 //               measured copy bandwidth at 8 x 64 MiB bf16, 99.9% at 8 x 256
 //               MiB; one CTA per SM or more gave 90-92%: fewer concurrent DRAM
 //               streams win); the fewest bytes per CTA stay at 512 so small
-//               calls spread over many CTAs.
+//               calls spread over many CTAs.  2 ranks: 3 CTAs of 256 threads
+//               per SM; more than 8: 256 CTAs of 256 threads.
 //   ReduceScatter  from 64 MiB per rank the TMA bulk ring (2 slots x 32 KiB
 //               per source), above the copy bandwidth from 128 MiB (the
 //               traffic is 8 reads per write); below, the register path with
@@ -147,7 +148,19 @@ Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
       t.unroll = world <= 4 ? 2 : 1;
       t.chunk_bytes = 64 * 1024;  // two-shot tile
       t.threads = 512;
-      if (S >= 8 * MiB) {
+      if (S >= 8 * MiB && world <= 2) {
+        // two sources: few bytes in flight per thread, so many more CTAs
+        // (6057 against 5082 GB/s for the 128-CTA setting at 2 x 64 MiB)
+        t.threads = 256;
+        t.ctas_per_sm = 3;
+        t.store_hint = 2;
+      } else if (S >= 8 * MiB && world > 8) {
+        // more than 8 sources: CTAs of 256 threads (the generic-count kernel's
+        // bound), 256 of them (6612 against 5312 GB/s for 128 at 16 x 64 MiB)
+        t.threads = 256;
+        t.max_ctas = 256;
+        t.store_hint = 2;
+      } else if (S >= 8 * MiB) {
         // 128 CTAs of 512 threads, one contiguous share each, evict-first
         // stores: fewer concurrent DRAM streams than one CTA per SM
         t.max_ctas = 128;
@@ -201,14 +214,15 @@ Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
         t.schedule = kSchedQueue;
         t.interleave_bytes = 32 * 1024;
       } else if (S >= 8 * MiB && coll == kAllGather) {
-        // one bulk load, eight bulk stores per chunk; 16 KiB parts from the
-        // shared queue, one CTA per SM
+        // one bulk load, `world` bulk stores per chunk, one CTA per SM, parts
+        // from the shared queue: 16 KiB with 3 slots for 8 ranks, 64 KiB with
+        // 4 slots for up to 4 (6283 against 4644 GB/s at 2 x 64 MiB)
         t.path = kPathBulk;
         t.ctas_per_sm = 1;
-        t.stages = 3;
+        t.stages = world <= 4 ? 4 : 3;
         t.chunk_bytes = 32 * 1024;
         t.schedule = kSchedQueue;
-        t.interleave_bytes = 16 * 1024;
+        t.interleave_bytes = world <= 4 ? 64 * 1024 : 16 * 1024;
       } else if (S >= 4 * MiB) {
         // one load, eight stores per vector: like the AllReduce, 128 CTAs of
         // 512 threads with evict-first stores
@@ -510,6 +524,9 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
     }
   }
   if (!p.reduce) p.nsrc = 1;
+  // the register-path kernel for more than 8 sources is built for CTAs of at
+  // most 256 threads (room for 128 registers)
+  if (p.tune.path == kPathRegister && p.nsrc > 8) p.tune.threads = std::min(p.tune.threads, 256);
   // Streamed schedules are copy plans on the bulk path.  The shared queue
   // serves every plan on the register path, and copy plans on the bulk path.
   if (p.tune.schedule == kSchedStream && (p.reduce || sync || p.tune.path != kPathBulk)) return PL_ERR_UNSUPPORTED;

@@ -282,41 +282,65 @@ __device__ __forceinline__ void reduce_elem(const char* const* src, int ns, char
   for (int j = 0; j < nd; ++j) Elem<T>::store(dst[j] + o, acc);
 }
 
+// Fold K sources (vectors v, v + step, ... of each) into acc: all K x UU
+// loads first, then the adds in source order.  FIRST: acc starts from the
+// first source's values.
+template <typename T, int K, int UU, bool FIRST, bool COHERENT>
+__device__ __forceinline__ void fold_batch(const char* const* src, uint64_t off, uint32_t v, uint32_t step,
+                                           float (&acc)[UU][Elem<T>::kPerVec]) {
+  constexpr int EPV = Elem<T>::kPerVec;
+  uint4 r[UU][K];
+#pragma unroll
+  for (int b = 0; b < K; ++b) {
+    const uint4* p = reinterpret_cast<const uint4*>(src[b] + off) + v;
+#pragma unroll
+    for (int u = 0; u < UU; ++u) r[u][b] = ld_vec<COHERENT>(p + u * step);
+  }
+#pragma unroll
+  for (int u = 0; u < UU; ++u) {
+#pragma unroll
+    for (int b = 0; b < K; ++b) {
+      if (FIRST && b == 0) {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) acc[u][e] = Elem<T>::get(r[u][b], e);
+      } else {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) acc[u][e] = __fadd_rn(acc[u][e], Elem<T>::get(r[u][b], e));
+      }
+    }
+  }
+}
+
+// Fold a run-time count of 1..8 sources, each count with its own unrolled code.
+template <typename T, int UU, bool FIRST, bool COHERENT>
+__device__ __forceinline__ void fold_up_to_8(const char* const* src, int k, uint64_t off, uint32_t v,
+                                             uint32_t step, float (&acc)[UU][Elem<T>::kPerVec]) {
+  switch (k) {
+    case 1: fold_batch<T, 1, UU, FIRST, COHERENT>(src, off, v, step, acc); break;
+    case 2: fold_batch<T, 2, UU, FIRST, COHERENT>(src, off, v, step, acc); break;
+    case 3: fold_batch<T, 3, UU, FIRST, COHERENT>(src, off, v, step, acc); break;
+    case 4: fold_batch<T, 4, UU, FIRST, COHERENT>(src, off, v, step, acc); break;
+    case 5: fold_batch<T, 5, UU, FIRST, COHERENT>(src, off, v, step, acc); break;
+    case 6: fold_batch<T, 6, UU, FIRST, COHERENT>(src, off, v, step, acc); break;
+    case 7: fold_batch<T, 7, UU, FIRST, COHERENT>(src, off, v, step, acc); break;
+    default: fold_batch<T, 8, UU, FIRST, COHERENT>(src, off, v, step, acc); break;
+  }
+}
+
 // UU vectors starting at index v (stride `step`) of every source: fold and
 // store.  NS > 0: exactly NS sources, all loads issued before the first add.
-// NS == 0: ns sources (up to 16), loaded in batches of 8.
+// NS == 0: ns sources (1..16): the first up to 8 as one batch, the rest as a
+// second, each batch with all its loads issued before its adds.
 template <typename T, int NS, int UU, bool STREAMING, bool COHERENT = false, int SW = 16>
 __device__ __forceinline__ void reduce_step(const char* const* src, int ns, char* const* dst, int nd,
                                             uint64_t off, uint32_t v, uint32_t step) {
   constexpr int EPV = Elem<T>::kPerVec;
-  constexpr int B = NS ? NS : 8;
-  const int nsrc = NS ? NS : ns;
   float acc[UU][EPV];
-  for (int s0 = 0; s0 < nsrc; s0 += B) {
-    uint4 r[UU][B];
-#pragma unroll
-    for (int b = 0; b < B; ++b) {
-      if (NS || s0 + b < nsrc) {
-        const uint4* p = reinterpret_cast<const uint4*>(src[s0 + b] + off) + v;
-#pragma unroll
-        for (int u = 0; u < UU; ++u) r[u][b] = ld_vec<COHERENT>(p + u * step);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < UU; ++u) {
-#pragma unroll
-      for (int b = 0; b < B; ++b) {
-        if (NS || s0 + b < nsrc) {
-          if (s0 + b == 0) {
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) acc[u][e] = Elem<T>::get(r[u][b], e);
-          } else {
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) acc[u][e] = __fadd_rn(acc[u][e], Elem<T>::get(r[u][b], e));
-          }
-        }
-      }
-    }
+  if constexpr (NS > 0) {
+    fold_batch<T, NS, UU, true, COHERENT>(src, off, v, step, acc);
+  } else {
+    fold_up_to_8<T, UU, true, COHERENT>(src, ns < 8 ? ns : 8, off, v, step, acc);
+    if (ns > 8) fold_up_to_8<T, UU, false, COHERENT>(src + 8, ns - 8, off, v, step, acc);
   }
 #pragma unroll
   for (int u = 0; u < UU; ++u) {
