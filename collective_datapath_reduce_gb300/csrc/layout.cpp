@@ -121,8 +121,8 @@ size_t n_sizes(int coll, int world) {
 //               (5889 against 5681 item by item).
 //   AllToAll    from 16 MiB per rank the queue in 64 KiB parts, 5 slots (7096
 //               against 6864 item by item at 256 MiB, 6800 against 6557 at 64
-//               MiB); AllToAllV from 32 MiB the queue in 192 KiB parts, 4
-//               slots (5923 against 5768).  Below, register copies with
+//               MiB); AllToAllV from 32 MiB the guided queue (parts
+//               shrinking to 64 KiB), 4 slots.  Below, register copies with
 //               streaming stores.
 //   Copy Atom, one destination: from 32 MiB the queue in 64 KiB parts (6973
 //               against 6762 GB/s item by item at 1 GiB); from 4 MiB, 8
@@ -237,13 +237,16 @@ Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
     case kAllToAll:
     case kAllToAllV:
       if (coll == kAllToAllV && S >= 32 * MiB) {
-        // mostly misaligned pieces: shifted bulk copies from the shared queue
+        // mostly misaligned pieces: shifted bulk copies from the guided queue
+        // (parts shrinking to 64 KiB: 6222 against 6036 GB/s for equal 192 KiB
+        // parts; the copies whose CTAs sweep the buffers together in small
+        // equal parts lose 7-11% with guided parts)
         t.path = kPathBulk;
         t.ctas_per_sm = 1;
         t.stages = 4;
         t.chunk_bytes = 32 * 1024;
-        t.schedule = kSchedQueue;
-        t.interleave_bytes = 192 * 1024;
+        t.schedule = kSchedQueueGuided;
+        t.interleave_bytes = 64 * 1024;
       } else if (coll == kAllToAll && S >= 16 * MiB) {
         // bulk ring of 5 slots fed from the shared queue in 64 KiB parts
         t.path = kPathBulk;
@@ -301,7 +304,7 @@ static int validate_tune(const Tune& t) {
   if (t.interleave_bytes < -1 || (t.interleave_bytes > 0 && (t.interleave_bytes < 512 || t.interleave_bytes % 512)))
     return PL_ERR_INVALID_ARG;
   if (t.max_ctas < 0) return PL_ERR_INVALID_ARG;
-  if (t.schedule < kSchedItem || t.schedule > kSchedQueue) return PL_ERR_INVALID_ARG;
+  if (t.schedule < kSchedItem || t.schedule > kSchedQueueGuided) return PL_ERR_INVALID_ARG;
   return PL_OK;
 }
 
@@ -530,7 +533,9 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
   // Streamed schedules are copy plans on the bulk path.  The shared queue
   // serves every plan on the register path, and copy plans on the bulk path.
   if (p.tune.schedule == kSchedStream && (p.reduce || sync || p.tune.path != kPathBulk)) return PL_ERR_UNSUPPORTED;
-  if (p.tune.schedule == kSchedQueue && p.tune.path == kPathBulk && (p.reduce || sync)) return PL_ERR_UNSUPPORTED;
+  if ((p.tune.schedule == kSchedQueue || p.tune.schedule == kSchedQueueGuided) && p.tune.path == kPathBulk &&
+      (p.reduce || sync))
+    return PL_ERR_UNSUPPORTED;
 
   // ------------------------------------------------------------ tiling
   uint64_t gcap = (uint64_t)p.tune.ctas_per_sm * (uint64_t)sm_count;
@@ -538,7 +543,7 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
   if (sync) {
     p.strided = true;
     p.sync = true;
-    p.queue = p.tune.schedule == kSchedQueue;
+    p.queue = p.tune.schedule == kSchedQueue || p.tune.schedule == kSchedQueueGuided;
     p.n_flags = (int)n_flags;
     const uint64_t n = pieces.size();
     p.grid = (int)std::max<uint64_t>(1, std::min<uint64_t>(gcap, n));
@@ -561,14 +566,34 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
     // shares of at least one 512-byte granule, except that pieces smaller than
     // that may each get a CTA of their own (latency of small calls)
     G = std::min<uint64_t>(G, std::max<uint64_t>({1, W / kSplitGranule, (uint64_t)pieces.size()}));
-    const bool queue = p.tune.schedule == kSchedQueue;
-    uint64_t k = 1;
-    if (p.tune.interleave_bytes > 0 || queue) {
+    const bool queue = p.tune.schedule == kSchedQueue || p.tune.schedule == kSchedQueueGuided;
+    // part ends in the concatenated piece space (the last one is W)
+    std::vector<uint64_t> ends;
+    if (p.tune.schedule == kSchedQueueGuided) {
+      // guided: each part is 1/(2 grid) of what is left, down to
+      // interleave_bytes: large parts first (few items), small ones last
+      // (the CTAs that run slower stop at nearly the same time)
       const uint64_t T = p.tune.interleave_bytes > 0 ? (uint64_t)p.tune.interleave_bytes : kQueuePartBytes;
-      k = std::max<uint64_t>(1, (W + T * G / 2) / (T * G));
-      k = std::min<uint64_t>(k, std::max<uint64_t>(1, W / (kSplitGranule * G)));
+      uint64_t pos = 0;
+      while (pos < W) {
+        uint64_t part = std::max<uint64_t>(T, (W - pos) / (2 * G));
+        part = (part + kSplitGranule - 1) & ~(kSplitGranule - 1);
+        pos = (W - pos <= part) ? W : pos + part;
+        ends.push_back(pos);
+      }
+    } else {
+      uint64_t k = 1;
+      if (p.tune.interleave_bytes > 0 || queue) {
+        const uint64_t T = p.tune.interleave_bytes > 0 ? (uint64_t)p.tune.interleave_bytes : kQueuePartBytes;
+        k = std::max<uint64_t>(1, (W + T * G / 2) / (T * G));
+        k = std::min<uint64_t>(k, std::max<uint64_t>(1, W / (kSplitGranule * G)));
+      }
+      const uint64_t n = k * G;
+      for (uint64_t j = 0; j < n; ++j)
+        // exact integer part boundary: floor((j+1) * W / n) without overflow
+        ends.push_back(j + 1 == n ? W : (uint64_t)(((unsigned __int128)(j + 1) * W) / n));
     }
-    const uint64_t nparts = k * G;
+    const uint64_t nparts = ends.size();
     p.queue = queue;
     p.grid = (int)G;
     std::vector<uint64_t> start(pieces.size() + 1, 0);
@@ -593,9 +618,7 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
         ep = pieces.size();
         eo = 0;
       } else {
-        // exact integer part boundary: floor((j+1) * W / nparts) without overflow
-        const uint64_t b = (uint64_t)(((unsigned __int128)(j + 1) * W) / nparts);
-        locate(b, ep, eo);
+        locate(ends[j], ep, eo);
       }
       // the shared queue hands out items in global order: one list
       std::vector<Item>& dst = per_cta[queue ? 0 : (size_t)(j % G)];

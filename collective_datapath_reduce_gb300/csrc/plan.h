@@ -44,8 +44,9 @@ enum Path : int { kPathRegister = 1, kPathBulk = 2 };
 // and drains its own pipeline).  Stream: a CTA's items flow through one
 // continuous bulk pipeline.  Queue: streamed, and the CTAs take items in
 // order from a counter shared by the grid instead of fixed shares.  Stream
-// and queue serve copy plans on the bulk path.
-enum Schedule : int { kSchedItem = 1, kSchedStream = 2, kSchedQueue = 3 };
+// and queue serve copy plans on the bulk path.  Guided queue: the queue with
+// parts that shrink toward the end of the work.
+enum Schedule : int { kSchedItem = 1, kSchedStream = 2, kSchedQueue = 3, kSchedQueueGuided = 4 };
 
 // Device format of one work item (40 bytes).  Same field meanings as
 // purlin_item in the public header, minus the CTA bookkeeping.

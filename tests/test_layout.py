@@ -287,7 +287,7 @@ def test_schedule_combinations():
         assert st(coll, dtype, [1 << 20], path=P.PATH_REGISTER, schedule=P.PL_SCHED_QUEUE) == P.PL_OK
     assert st(AR, P.PL_F32, [1 << 20], path=P.PATH_REGISTER, schedule=P.PL_SCHED_QUEUE,
               layout=P.PL_LAYOUT_TWO_SHOT) == P.PL_OK
-    assert st(AG, P.PL_U8, [1 << 20], schedule=4) == P.PL_ERR_INVALID_ARG
+    assert st(AG, P.PL_U8, [1 << 20], schedule=5) == P.PL_ERR_INVALID_ARG
 
 
 def test_queued_two_shot_plan_orders_every_wait_after_its_notify():
@@ -312,3 +312,32 @@ def test_queued_two_shot_plan_orders_every_wait_after_its_notify():
         want = oracle.all_reduce(ins, "f32")
         for r in range(world):
             assert np.array_equal(outs[r], _bytes(want[r]))
+
+
+def test_guided_queue_plans():
+    """Guided queue: parts shrink from 1/(2 grid) of the work to the minimum,
+    items in global order, same coverage as any other plan."""
+    world = 8
+    C = RNG.integers(0, 200000, size=(world, world))
+    tune = {"path": P.PATH_BULK, "schedule": P.PL_SCHED_QUEUE_GUIDED, "interleave_bytes": 8192}
+    sres, dres = _res(world, False), _res(world, False)
+    src_addr = [0x1000000 * (r + 1) + sres[r] for r in range(world)]
+    dst_addr = [0x9000000 * (r + 1) + dres[r] for r in range(world)]
+    st, items, grid, _ = P.purlin_plan_describe(P.PL_COLL_ALL_TO_ALL_V, world, P.PL_U8, C.reshape(-1).tolist(),
+                                                src_addr, dst_addr, 152, tune)
+    assert st == P.PL_OK
+    assert all(it["cta"] == QUEUED for it in items)
+    W = int(C.sum())
+    lens = [it["len"] for it in items]
+    assert lens[0] >= W // (2 * grid) - 512 or lens[0] < 8192      # the first part is large
+    assert max(lens[-20:]) <= 8192 + 512                          # the last ones are the minimum
+    ins = [RNG.integers(0, 256, size=int(C[s].sum()), dtype=np.uint8) for s in range(world)]
+    outs = [np.zeros(int(C[:, d].sum()), np.uint8) for d in range(world)]
+    run_items(items, ins, outs, "u8")
+    want = oracle.all_to_all_v(ins, C)
+    for r in range(world):
+        assert np.array_equal(outs[r], want[r])
+    # the register path takes it too (every plan), a two-shot SNAC plan included
+    st, items, _, _ = P.purlin_plan_describe(P.PL_COLL_ALL_REDUCE, world, P.PL_F32, [1 << 22], None, None, 152,
+                                             {"schedule": P.PL_SCHED_QUEUE_GUIDED, "interleave_bytes": 4096})
+    assert st == P.PL_OK and items[0]["len"] > items[-1]["len"]
