@@ -61,7 +61,7 @@ def expect(outs, want, view=None):
             assert np.array_equal(got, w), r
 
 
-SCHED = [P.PL_SCHED_STREAM, P.PL_SCHED_QUEUE]
+SCHED = [P.PL_SCHED_STREAM, P.PL_SCHED_QUEUE, P.PL_SCHED_QUEUE_GUIDED]
 
 
 @pytest.mark.parametrize("schedule", SCHED)
