@@ -550,6 +550,19 @@ def side_table(P, h, stream, dev):
             lambda: chk(P.purlin_reduce_scatter(h, x, y, size, P.PL_F32, 0, stream))), size)
         del x, y
         torch.cuda.empty_cache()
+    # the allocation-free AllReduce entry point (two-shot, scratch in a static
+    # device array; no handle), timed in plain launches
+    out["all_reduce_noalloc_bf16"] = {}
+    dstat = torch.zeros(1, dtype=torch.int32, device=dev)
+    for size in (16 * MI, 64 * MI, 256 * MI):
+        x = bufs(size // 2, WORLD, torch.bfloat16)
+        y = [torch.empty_like(t) for t in x]
+        out["all_reduce_noalloc_bf16"][f"{size >> 20}MiB"] = point(2 * WORLD * size, timeit(
+            lambda: chk(P.purlin_all_reduce_noalloc(WORLD, x, y, size, P.PL_BF16, dstat, stream)), graph=False), size)
+        if int(dstat.item()) != 0:
+            raise RuntimeError("allocation-free AllReduce reported a device error")
+        del x, y
+    torch.cuda.empty_cache()
     # ReduceScatterV: uneven chunks (workload 5's first row of counts), bf16
     from collective_datapath_reduce_gb300 import inputs as _inputs
     C5, _ = _inputs.w5_counts(WORLD)

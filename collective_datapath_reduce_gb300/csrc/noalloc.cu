@@ -257,7 +257,9 @@ extern "C" purlin_status purlin_all_reduce_noalloc(int world, const void* const*
   a.elem = (uint32_t)E;
   a.world = (uint32_t)world;
   a.tmax = (uint32_t)tmax;
-  a.lag = (uint32_t)std::max<uint64_t>(1, ((uint64_t)ctas + 2ull * world - 1) / (2ull * world));
+  // copies trail their reduce by about two waves of CTAs (as the library's
+  // two-shot plans): the reduce has usually finished when its copies start
+  a.lag = (uint32_t)std::max<uint64_t>(1, ((uint64_t)ctas + world - 1) / (uint64_t)world);
   a.slots = (uint32_t)((tmax + a.lag) * 2ull * (uint64_t)world);
   a.dst_coaligned = same;
   const int grid = (int)std::min<uint64_t>((uint64_t)ctas, a.slots);
