@@ -68,3 +68,23 @@ def test_torch_front_end_matches_oracle():
             assert np.array_equal(agv[r].cpu().numpy(), want_g[r])
     finally:
         purlin.finalize(h)
+
+
+@pytest.mark.gpu
+def test_torch_front_end_takes_pinned_host_tensors():
+    """Pinned host tensors go to the kernels as they are (read and written in place)."""
+    dev = torch.device("cuda", 0)
+    world, n = 4, 50021
+    rng = np.random.default_rng(6)
+    h = purlin.initialize(world, dev)
+    try:
+        f = [rng.standard_normal(n).astype(np.float32) for _ in range(world)]
+        xs = [torch.from_numpy(a.copy()).pin_memory() for a in f]
+        outs = [torch.empty(n).pin_memory() for _ in range(world)]
+        purlin.all_reduce(xs, outs, h)
+        torch.cuda.synchronize()
+        want = oracle.all_reduce(f, "f32")
+        for r in range(world):
+            assert np.array_equal(outs[r].numpy().view(np.uint32), want[r].view(np.uint32))
+    finally:
+        purlin.finalize(h)
