@@ -38,9 +38,12 @@ def chain(h, base, x, y, z, s, rounds, call):
             torch.sum(y[r].double(), dim=0, keepdim=True, out=z[r][k:k + 1])
 
 
-@pytest.mark.parametrize("kind", ["all_reduce", "all_gather", "all_to_all"])
-def test_producer_call_consumer_chain(kind):
-    world, n, rounds = 8, (1 << 20) + 8, 12
+@pytest.mark.parametrize("kind,n", [("all_reduce", (1 << 20) + 8), ("all_gather", (1 << 20) + 8),
+                                    ("all_to_all", (1 << 20) + 8),
+                                    # sizes the table runs on the streamed bulk kernel
+                                    ("all_gather", (1 << 21) + 8), ("all_to_all", (1 << 22) + 8)])
+def test_producer_call_consumer_chain(kind, n):
+    world, rounds = 8, 12
     dev = torch.device("cuda", 0)
     g = torch.Generator(device=dev)
     g.manual_seed(11)
