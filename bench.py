@@ -47,10 +47,11 @@ WORKLOAD = "AllReduce sum, 8 emulated ranks on one GPU, bf16 in/out, fp32 ascend
 class Workload:
     """One collective at one workload size: host inputs, output sizes, the call, its bytes."""
 
-    def __init__(self, name, desc, dtype, make_inputs, out_bytes, call, algo_bytes, coll, tune_bytes):
+    def __init__(self, name, desc, dtype, make_inputs, out_bytes, call, algo_bytes, coll, tune_bytes, tune=None):
         self.name, self.desc, self.dtype = name, desc, dtype
         self.make_inputs, self.out_bytes, self.call = make_inputs, out_bytes, call
         self.algo_bytes, self.coll, self.tune_bytes = algo_bytes, coll, tune_bytes
+        self.tune = tune  # tuning override applied to the handle (None: the table's choice)
 
 
 def workloads(P, inputs):
@@ -62,6 +63,12 @@ def workloads(P, inputs):
                  lambda: list(inputs.w2_allreduce_bf16(WORLD, N_ELEMS, seed=1)),
                  [S] * WORLD, lambda h, s, d, st: P.purlin_all_reduce(h, s, d, S, P.PL_BF16, 0, st),
                  ALGO_BYTES, P.PL_COLL_ALL_REDUCE, S),
+        Workload("allreduce_two_shot_bf16_8x64MiB", WORKLOAD.replace("AllReduce sum", "AllReduce sum, two-shot "
+                 "layout (each owner reduces its range, notifies, and the range is copied to the other ranks: "
+                 "SNAC between CTAs),", 1), "bf16",
+                 lambda: list(inputs.w2_allreduce_bf16(WORLD, N_ELEMS, seed=1)),
+                 [S] * WORLD, lambda h, s, d, st: P.purlin_all_reduce(h, s, d, S, P.PL_BF16, 0, st),
+                 ALGO_BYTES, P.PL_COLL_ALL_REDUCE, S, tune={"layout": P.PL_LAYOUT_TWO_SHOT}),
         Workload("reduce_scatter_f32_8x256MiB",
                  "ReduceScatter sum, 8 ranks, fp32, 64 Mi elements (256 MiB) per rank, U(-1,1), seed 2", "f32",
                  lambda: list(inputs.w3_reduce_scatter(WORLD, 64 * MI, seed=2, dtype="f32")),
@@ -274,6 +281,9 @@ def run_own(args, dist):
 
     _, tune = P.purlin_tune_get(h, wl.coll, {"bf16": P.PL_BF16, "f32": P.PL_F32, "u8": P.PL_U8}[wl.dtype],
                                 wl.tune_bytes)
+    if wl.tune:
+        P.check(P.purlin_tune_override(h, wl.tune), "purlin_tune_override")
+        tune.update(wl.tune)
     # The clock sampler starts first; the warm-up steps then run straight into
     # the timed region, so the GPU does not sit idle (and clock down) in between.
     clocks = ClockSampler(dist.local)
