@@ -279,11 +279,10 @@ def run_own(args, dist):
         if st != P.PL_OK:
             raise P.PurlinError(st, wl.name)
 
-    _, tune = P.purlin_tune_get(h, wl.coll, {"bf16": P.PL_BF16, "f32": P.PL_F32, "u8": P.PL_U8}[wl.dtype],
-                                wl.tune_bytes)
     if wl.tune:
         P.check(P.purlin_tune_override(h, wl.tune), "purlin_tune_override")
-        tune.update(wl.tune)
+    _, tune = P.purlin_tune_get(h, wl.coll, {"bf16": P.PL_BF16, "f32": P.PL_F32, "u8": P.PL_U8}[wl.dtype],
+                                wl.tune_bytes)
     # The clock sampler starts first; the warm-up steps then run straight into
     # the timed region, so the GPU does not sit idle (and clock down) in between.
     clocks = ClockSampler(dist.local)

@@ -726,8 +726,11 @@ purlin_status purlin_tune_get(purlin_handle h, purlin_coll coll, purlin_dtype dt
   purlin_status st;
   if ((st = check_handle(h))) return st;
   if (!out) return PL_ERR_INVALID_ARG;
-  pl::Tune t = pl::tune_table(coll, h->world, dtype, bytes_per_rank);
-  if (h->has_over) t = pl::tune_merge(t, h->over);
+  const pl::Tune over = h->has_over ? h->over : pl::Tune{};
+  pl::Tune t = pl::resolve_tune(coll, coll, h->world, dtype, bytes_per_rank, over);
+  const bool reduce = coll == PL_COLL_ALL_REDUCE || coll == PL_COLL_REDUCE_SCATTER ||
+                      coll == PL_COLL_REDUCE_SCATTER_V;
+  if (t.path == pl::kPathRegister && reduce && h->world > 8) t.threads = std::min(t.threads, 256);
   static_assert(sizeof(pl::Tune) == sizeof(purlin_tune), "tune layout");
   std::memcpy(out, &t, sizeof t);
   return PL_OK;

@@ -291,6 +291,19 @@ Tune tune_merge(const Tune& b, const Tune& o) {
   return t;
 }
 
+Tune resolve_tune(int coll, int table_coll, int world, int dtype, uint64_t bytes_per_rank, const Tune& over) {
+  Tune t = tune_merge(tune_table(table_coll, world, dtype, bytes_per_rank), over);
+  if (coll == kAllReduce && t.layout == kTwoShot) {
+    // the two-shot layout's own best (512 threads, two CTAs per SM, write-back
+    // stores, no grid cap) unless the caller set these fields
+    if (!over.threads) t.threads = 512;
+    if (!over.ctas_per_sm) t.ctas_per_sm = 2;
+    if (!over.store_hint) t.store_hint = 1;
+    if (!over.max_ctas) t.max_ctas = 0;
+  }
+  return t;
+}
+
 static int validate_tune(const Tune& t) {
   if (t.layout < kOneShot || t.layout > kTwoShot) return PL_ERR_UNSUPPORTED;
   if (t.threads < 64 || t.threads > 512 || t.threads % 32) return PL_ERR_INVALID_ARG;
@@ -339,15 +352,7 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
   // A reduce Atom with one destination moves ReduceScatter-shaped traffic
   // (N reads per write); with several it is AllReduce-shaped.
   const int table_coll = (coll == kAtomReduce && nsizes == 3 && sizes[2] == 1) ? (int)kReduceScatter : coll;
-  p.tune = tune_merge(tune_table(table_coll, world, dtype, per_rank), tune_in);
-  if (coll == kAllReduce && p.tune.layout == kTwoShot) {
-    // the two-shot layout's own best (512 threads, two CTAs per SM, write-back
-    // stores, no grid cap) unless the caller set these fields
-    if (!tune_in.threads) p.tune.threads = 512;
-    if (!tune_in.ctas_per_sm) p.tune.ctas_per_sm = 2;
-    if (!tune_in.store_hint) p.tune.store_hint = 1;
-    if (!tune_in.max_ctas) p.tune.max_ctas = 0;
-  }
+  p.tune = resolve_tune(coll, table_coll, world, dtype, per_rank, tune_in);
   if (int st = validate_tune(p.tune)) return st;
   if (p.tune.interleave_bytes < 0) p.tune.interleave_bytes = 0;  // -1 in an override: contiguous shares
   if (max_ctas_per_sm > 0) p.tune.ctas_per_sm = std::min(p.tune.ctas_per_sm, max_ctas_per_sm);

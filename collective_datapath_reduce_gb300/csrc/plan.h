@@ -104,6 +104,11 @@ int elem_size(int dtype);
 Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank);
 // Fill zero fields of `over` from `base`.
 Tune tune_merge(const Tune& base, const Tune& over);
+// The tuning a call runs with: the table entry (of `table_coll`), then the
+// override, then the layout's own defaults (two-shot AllReduce).  The plan
+// may still cap the thread count (more than 8 sources on the register path)
+// and the CTAs per SM (co-residency of SNAC plans).
+Tune resolve_tune(int coll, int table_coll, int world, int dtype, uint64_t bytes_per_rank, const Tune& over);
 
 // Build the plan.  src_res / dst_res: address of each rank's buffer modulo 16
 // (world entries).  max_ctas_per_sm caps tune.ctas_per_sm (residency limit

@@ -249,7 +249,9 @@ purlin_status purlin_status_get(purlin_handle h, purlin_stream_t stream, int* de
 
 const char* purlin_status_string(purlin_status s);
 
-/* The tuning the handle would use for a call (table entry, then override). */
+/* The tuning the handle would use for a call: table entry, then the
+ * handle's override, then the layout's own defaults (two-shot AllReduce) and
+ * the thread cap of the register path beyond 8 sources. */
 purlin_status purlin_tune_get(purlin_handle h, purlin_coll coll, purlin_dtype dtype,
                               size_t bytes_per_rank, purlin_tune* out);
 
