@@ -1,6 +1,11 @@
 // TMA bulk datapath (sm_90+ `cp.async.bulk`, used here on sm_103a): the
-// staged alternative to the register path, for work items whose addresses
-// are all 16-byte aligned.
+// staged alternative to the register path, one work item at a time.  Items
+// whose addresses are all 16-byte aligned go through the bulk engines alone;
+// copies from a source misaligned against its destinations load aligned
+// windows and realign them in shared memory (bulk_copy_shifted_body); other
+// misaligned reductions fall back to the register Atoms.  The streamed
+// variant for copies (one pipeline across a CTA's items, optional shared
+// item queue) is kernels_stream.cu.
 //
 // Purlin 0.6.5 (PyPI page), "Samples": an Atom copies one aligned slice
 // through a pipeline in dynamic shared memory (COPY_PIPELINE_SMEM_BYTES).
