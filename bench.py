@@ -463,6 +463,7 @@ def side_table(P, h, stream, dev):
     GRAPH, WARM, RUNS = 10, 5, 20
     MI = 1 << 20
     l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * MI))
+    peak, _ = measured_peaks()
     flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
 
     def timeit(fn, graph=True):
@@ -512,7 +513,8 @@ def side_table(P, h, stream, dev):
         med = statistics.median(t)
         pct = lambda q: t[min(len(t) - 1, int(q * (len(t) - 1) + 0.5))]
         d = {"bytes": nbytes, "us": round(med * 1e3, 2), "us_p10": round(pct(0.1) * 1e3, 2),
-             "us_p90": round(pct(0.9) * 1e3, 2), "GB/s": round(nbytes / (med / 1e3) / 1e9, 1)}
+             "us_p90": round(pct(0.9) * 1e3, 2), "GB/s": round(nbytes / (med / 1e3) / 1e9, 1),
+             "pct_of_peak": round(100 * nbytes / (med / 1e3) / 1e9 / peak, 1)}
         if total_bytes is not None:
             d["totalBytes_GB/s"] = round(total_bytes / (med / 1e3) / 1e9, 1)
         if nbytes <= l2:
