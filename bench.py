@@ -662,30 +662,69 @@ def cpu_baseline(x, budget_s=12.0):
 
 # ----------------------------------------------------------- reference arm
 
+def _reference_call(name):
+    """The oracle function of a workload: f(list of rank arrays) -> outputs."""
+    import oracle
+    from collective_datapath_reduce_gb300 import inputs
+    C5, c5 = inputs.w5_counts(WORLD)
+    return {
+        "allreduce_bf16_8x64MiB": lambda ins: oracle.all_reduce(ins, "bf16"),
+        "allreduce_two_shot_bf16_8x64MiB": lambda ins: oracle.all_reduce(ins, "bf16"),
+        "reduce_scatter_f32_8x256MiB": lambda ins: oracle.reduce_scatter(ins, "f32"),
+        "reduce_scatter_bf16_8x128MiB": lambda ins: oracle.reduce_scatter(ins, "bf16"),
+        "all_gather_u8_8x256MiB": oracle.all_gather,
+        "all_to_all_u8_8x256MiB": oracle.all_to_all,
+        "all_to_all_v_bf16_w5": lambda ins: oracle.all_to_all_v(ins, C5),
+        "all_gather_v_bf16_w5": lambda ins: oracle.all_gather_v(ins, [int(v) for v in c5]),
+    }[name]
+
+
 def run_reference(args, dist):
-    """The oracle times itself on the host cores; rank 0 only."""
+    """The oracle of the selected workload times itself on the host cores, on
+    a bounded sample (the first elements of every rank; the V workloads in
+    full); rank 0 only."""
     if dist.rank != 0:
         return
     from collective_datapath_reduce_gb300 import inputs
-    n_total = N_ELEMS
-    x = inputs.w2_allreduce_bf16(WORLD, n_total, seed=1)
-    t = _oracle_sample(x, 1 << 20)
-    steps = args.steps + args.warmup
-    per_step_budget = max(0.05, 120.0 / max(steps, 1))
-    n_sample = int(min(n_total, max(1 << 16, (1 << 20) * per_step_budget / max(t, 1e-4))))
-    n_sample -= n_sample % 8
+    from collective_datapath_reduce_gb300 import purlin as P  # names only: the library is not loaded
+    wl = workloads(P, inputs)[args.workload]
+    fn = _reference_call(wl.name)
+    x = [np.asarray(a) for a in wl.make_inputs()]
+    full = sum(a.size for a in x)
+    if wl.name.endswith("_w5"):
+        def run(_k):
+            t0 = time.perf_counter()
+            fn(x)
+            return time.perf_counter() - t0
+        k_sample, frac = None, 1.0
+    else:
+        def run(k):
+            ins = [a[:k] for a in x]
+            t0 = time.perf_counter()
+            fn(ins)
+            return time.perf_counter() - t0
+        n = x[0].size
+        probe = min(n, 1 << 20)
+        t = run(probe - probe % (8 * WORLD))
+        steps = args.steps + args.warmup
+        per_step_budget = max(0.05, 120.0 / max(steps, 1))
+        k_sample = int(min(n, max(1 << 16, probe * per_step_budget / max(t, 1e-4))))
+        k_sample -= k_sample % (8 * WORLD)            # whole chunks for ReduceScatter / AllToAll
+        frac = k_sample / n
     for _ in range(args.warmup):
-        _oracle_sample(x, n_sample)
-    times = [_oracle_sample(x, n_sample) for _ in range(args.steps)]
+        run(k_sample)
+    times = [run(k_sample) for _ in range(args.steps)]
     per = sum(times) / len(times)
-    nbytes = 2 * WORLD * n_sample * ELEM
-    value = round(nbytes / per / 1e9, 4)
-    sample = f"first {n_sample} of {n_total} elements of each of the {WORLD} ranks per step (numpy, single-threaded)"
+    value = round(wl.algo_bytes * frac / per / 1e9, 4)
+    sample = ("the whole workload per step" if k_sample is None else
+              f"first {k_sample} of {x[0].size} elements of each of the {WORLD} ranks per step") + \
+        " (numpy, single-threaded)"
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per * 1e3, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "world": WORLD, "bytes_per_rank": S, "sampled_elements_per_rank": n_sample},
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.desc, "name": wl.name, "world": WORLD, "algorithmic_bytes_per_step": wl.algo_bytes,
+                   "sampled_fraction": round(frac, 6), "input_elements": full},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
