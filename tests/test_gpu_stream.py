@@ -321,3 +321,15 @@ def test_queued_two_shot_in_a_cuda_graph():
         assert h.status() == 0
     finally:
         assert h.close() == P.PL_OK
+
+
+@pytest.mark.parametrize("schedule", SCHED)
+def test_stream_sixteen_ranks(schedule):
+    """Sixteen destinations per AllGather item (every pointer slot of an item)."""
+    tune = {"path": P.PATH_BULK, "schedule": schedule, "stages": 3, "chunk_bytes": 8192, "interleave_bytes": 8192}
+    world = 16
+    for S in (48, 65536 + 16 * 3):
+        ins = [RNG.integers(0, 256, size=S, dtype=np.uint8) for _ in range(world)]
+        expect(run_twice("ag", world, ins, S, [world * S] * world, tune, [r % 16 for r in range(world)]),
+               oracle.all_gather(ins))
+        expect(run_twice("a2a", world, ins, S, [S] * world, tune), oracle.all_to_all(ins))
