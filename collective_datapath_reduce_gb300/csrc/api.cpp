@@ -48,7 +48,6 @@ struct purlin_ctx {
   int sm_count = 0;
   int arch = 0;
   int max_ctas_per_sm = 0;
-  int pageable_access = 0;   // the device can address pageable host memory
   void* ws = nullptr;
   size_t ws_bytes = 0;
   bool ws_owned = false;
@@ -282,8 +281,10 @@ purlin_status get_plan(purlin_ctx* h, int coll, int world, int dtype, const uint
 // Where one rank buffer lives, and the address the kernel uses for it.
 // Device and managed memory take every path.  Host memory the device maps
 // (cudaHostAlloc, cudaHostRegister) is read and written in place over the
-// host link; pageable host memory only where the device can address it.
-// Anything else (another device's memory, an unknown address) is refused.
+// host link.  Anything else is refused: another device's memory, and any
+// address the driver does not know -- even where the device could reach
+// pageable memory, an unknown address may not be a mapping at all, and the
+// kernel would fault on it.
 purlin_status locate(const purlin_ctx* h, const void* p, const void** dev_p, bool* host) {
   *dev_p = p;
   if (!p) return PL_OK;  // a zero-byte rank of a V collective
@@ -302,10 +303,8 @@ purlin_status locate(const purlin_ctx* h, const void* p, const void** dev_p, boo
       if (at.devicePointer) *dev_p = at.devicePointer;
       *host = true;
       return PL_OK;
-    default:  // unregistered host memory
-      if (!h->pageable_access) return PL_ERR_INVALID_ARG;
-      *host = true;
-      return PL_OK;
+    default:  // unregistered: pageable host memory, or no mapping at all
+      return PL_ERR_INVALID_ARG;
   }
 }
 
@@ -473,8 +472,6 @@ purlin_status purlin_initialize(int world, void* workspace, size_t workspace_byt
       (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, h->device)) != cudaSuccess)
     return cuda_fail(e);
   h->arch = major * 10 + minor;
-  if ((e = cudaDeviceGetAttribute(&h->pageable_access, cudaDevAttrPageableMemoryAccess, h->device)) != cudaSuccess)
-    return cuda_fail(e);
   const void* probe = pl::kernel_reduce_bf16(8, 1);
   if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&h->max_ctas_per_sm, probe, 512, 0)) != cudaSuccess)
     return cuda_fail(e);

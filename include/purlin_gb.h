@@ -20,12 +20,12 @@
  * Conventions shared by every entry point:
  *   - Pointers in src[] / dst[] are owned by the caller and point to memory
  *     the handle's device can address: its own device memory, managed
- *     memory, or host memory -- pinned (cudaHostAlloc, cudaHostRegister), or
- *     pageable where the device has pageable memory access.  The kernel reads
- *     and writes host memory in place over the host link (no staging copies;
- *     such calls run on the register path).  Any other pointer returns
- *     PL_ERR_INVALID_ARG.  The host arrays src[], dst[], bytes[] are read
- *     during the call only.
+ *     memory, or pinned host memory (cudaHostAlloc, or pageable memory after
+ *     cudaHostRegister).  The kernel reads and writes host memory in place
+ *     over the host link (no staging copies; such calls run on the register
+ *     path).  Any other pointer -- unregistered pageable memory included --
+ *     returns PL_ERR_INVALID_ARG.  The host arrays src[], dst[], bytes[] are
+ *     read during the call only.
  *   - `bytes` arguments count bytes, not elements.
  *   - Every collective is asynchronous on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream).  Argument errors are returned at once and
