@@ -372,6 +372,9 @@ def test_argument_errors():
     assert P.purlin_reduce_scatter(h.h, src.ptrs(), dst.ptrs(), 12, P.PL_F32, 0, S) == P.PL_ERR_INVALID_ARG
     assert P.purlin_all_to_all(h.h, src.ptrs(), dst.ptrs(), 10, S) == P.PL_ERR_INVALID_ARG
     assert P.purlin_all_reduce(h.h, [0] * world, dst.ptrs(), 64, P.PL_F32, 0, S) == P.PL_ERR_INVALID_ARG
+    # an address the driver does not know is refused before any launch
+    assert P.purlin_all_reduce(h.h, [0x10000 * (r + 1) for r in range(world)], dst.ptrs(), 64, P.PL_F32, 0,
+                               S) == P.PL_ERR_INVALID_ARG
     assert P.purlin_all_reduce(h.h, src.ptrs(), dst.ptrs(), 0, P.PL_F32, 0, S) == P.PL_OK  # zero bytes: no launch
     hh = h.h
     assert h.close() == P.PL_OK
