@@ -751,6 +751,7 @@ purlin_status purlin_set_wait_timeout_ns(purlin_handle h, uint64_t ns) {
   purlin_status st;
   if ((st = check_handle(h))) return st;
   if (ns == 0) return PL_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(h->mu);
   h->timeout_ns = ns;
   return PL_OK;
 }
@@ -758,6 +759,7 @@ purlin_status purlin_set_wait_timeout_ns(purlin_handle h, uint64_t ns) {
 purlin_status purlin_debug_drop_notify(purlin_handle h, long long item) {
   purlin_status st;
   if ((st = check_handle(h))) return st;
+  std::lock_guard<std::mutex> lock(h->mu);
   h->drop_notify = item < 0 ? -1 : item;
   return PL_OK;
 }
