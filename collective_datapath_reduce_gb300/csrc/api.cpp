@@ -119,9 +119,14 @@ bool overlaps(const Range& a, const Range& b) {
 }
 
 // Destinations must be pairwise disjoint and must not overlap any source,
-// except an exact in-place pair src[r] == dst[r] when allowed.
+// except an exact in-place pair src[r] == dst[r] when allowed.  A buffer whose
+// end would pass the top of the address space is refused too.
 purlin_status check_overlap(const std::vector<Range>& src, const std::vector<Range>& dst,
                             bool allow_in_place) {
+  for (const Range& r : src)
+    if (r.hi < r.lo) return PL_ERR_INVALID_ARG;
+  for (const Range& r : dst)
+    if (r.hi < r.lo) return PL_ERR_INVALID_ARG;
   for (size_t i = 0; i < dst.size(); ++i) {
     for (size_t j = i + 1; j < dst.size(); ++j)
       if (overlaps(dst[i], dst[j])) return PL_ERR_INVALID_ARG;
@@ -436,6 +441,9 @@ purlin_status check_elem_aligned(const void* const* p, int n, size_t e) {
   return PL_OK;
 }
 
+// a + b, or false where the sum does not fit in 64 bits
+bool add_u64(uint64_t a, uint64_t b, uint64_t* sum) { return !__builtin_add_overflow(a, b, sum); }
+
 std::vector<Range> ranges(const void* const* p, int n, const std::vector<uint64_t>& bytes) {
   std::vector<Range> r((size_t)n);
   for (int i = 0; i < n; ++i) r[i] = Range{(uintptr_t)p[i], (uintptr_t)p[i] + (uintptr_t)bytes[i]};
@@ -574,7 +582,7 @@ purlin_status purlin_reduce_scatter_v(purlin_handle h, const void* const* src, v
   for (int r = 0; r < N; ++r) {
     if (bytes[r] % E) return PL_ERR_ALIGNMENT;
     sz[r] = bytes[r];
-    total += bytes[r];
+    if (!add_u64(total, bytes[r], &total)) return PL_ERR_INVALID_ARG;
   }
   std::fill(bi.begin(), bi.end(), total);
   if ((st = check_ptrs_sized(src, N, bi)) || (st = check_ptrs_sized((const void* const*)dst, N, sz))) return st;
@@ -592,6 +600,7 @@ purlin_status purlin_all_gather(purlin_handle h, const void* const* src, void* c
   const int N = h->world;
   if ((st = check_ptrs(src, N)) || (st = check_ptrs((const void* const*)dst, N))) return st;
   if (in_bytes_per_rank == 0) return PL_OK;
+  if (in_bytes_per_rank > UINT64_MAX / (uint64_t)N) return PL_ERR_INVALID_ARG;  // outputs of world x bytes
   std::vector<uint64_t> bi((size_t)N, in_bytes_per_rank), bo((size_t)N, in_bytes_per_rank * N);
   if ((st = check_overlap(ranges(src, N, bi), ranges((const void* const*)dst, N, bo), false))) return st;
   const uint64_t sz = in_bytes_per_rank;
@@ -622,7 +631,7 @@ purlin_status purlin_all_gather_v(purlin_handle h, const void* const* src, void*
   uint64_t total = 0;
   for (int r = 0; r < N; ++r) {
     sz[r] = bytes[r];
-    total += bytes[r];
+    if (!add_u64(total, bytes[r], &total)) return PL_ERR_INVALID_ARG;
   }
   std::fill(bo.begin(), bo.end(), total);
   if ((st = check_ptrs_sized(src, N, sz)) || (st = check_ptrs_sized((const void* const*)dst, N, bo))) return st;
@@ -643,9 +652,8 @@ purlin_status purlin_all_to_all_v(purlin_handle h, const void* const* src, void*
     for (int d = 0; d < N; ++d) {
       const uint64_t c = bytes[(size_t)s * N + d];
       sz[(size_t)s * N + d] = c;
-      bi[s] += c;
-      bo[d] += c;
-      total += c;
+      if (!add_u64(bi[s], c, &bi[s]) || !add_u64(bo[d], c, &bo[d]) || !add_u64(total, c, &total))
+        return PL_ERR_INVALID_ARG;
     }
   if ((st = check_ptrs_sized(src, N, bi)) || (st = check_ptrs_sized((const void* const*)dst, N, bo))) return st;
   if (total == 0) return PL_OK;

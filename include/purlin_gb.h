@@ -35,6 +35,10 @@
  *   - A call that moves zero bytes returns PL_OK without launching anything.
  *   - Destination ranges must not overlap each other or any source range.
  *     The one exception is in-place AllReduce, src[r] == dst[r].
+ *   - Sizes whose sums (a V collective's totals, an AllGather's world x bytes)
+ *     or whose buffer ends do not fit in 64 bits return PL_ERR_INVALID_ARG.
+ *     The library cannot see how large the caller's allocations are: byte
+ *     counts larger than the buffers they describe are the caller's error.
  *   - Reductions need every pointer aligned to the element size; copies take
  *     any byte alignment.  16-byte alignment of every address is the fast path.
  *   - Calls on one handle must be ordered (one stream, or streams the caller
@@ -62,7 +66,7 @@ typedef void* purlin_stream_t; /* a cudaStream_t */
 
 typedef enum {
   PL_OK = 0,
-  PL_ERR_INVALID_ARG = 1,  /* null pointer, bad world, sizes that do not split, overlap */
+  PL_ERR_INVALID_ARG = 1,  /* null pointer, bad world, sizes that do not split or overflow, overlap */
   PL_ERR_ALIGNMENT = 2,    /* a reduce pointer or size not aligned to the element size */
   PL_ERR_UNSUPPORTED = 3,  /* e.g. a reduction over PL_U8, an unknown mode or layout */
   PL_ERR_WORKSPACE = 4,    /* caller-provided workspace too small for this call */

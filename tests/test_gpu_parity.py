@@ -376,6 +376,14 @@ def test_argument_errors():
     assert P.purlin_all_reduce(h.h, [0x10000 * (r + 1) for r in range(world)], dst.ptrs(), 64, P.PL_F32, 0,
                                S) == P.PL_ERR_INVALID_ARG
     assert P.purlin_all_reduce(h.h, src.ptrs(), dst.ptrs(), 0, P.PL_F32, 0, S) == P.PL_OK  # zero bytes: no launch
+    # sizes whose totals or buffer ends do not fit in 64 bits are refused before any launch
+    huge = (1 << 64) - 16
+    assert P.purlin_all_reduce(h.h, src.ptrs(), dst.ptrs(), huge, P.PL_F32, 0, S) == P.PL_ERR_INVALID_ARG
+    assert P.purlin_all_gather(h.h, src.ptrs(), dst.ptrs(), 1 << 62, S) == P.PL_ERR_INVALID_ARG
+    assert P.purlin_all_gather_v(h.h, src.ptrs(), dst.ptrs(), [1 << 63, 1 << 63, 16, 16], S) == P.PL_ERR_INVALID_ARG
+    assert P.purlin_all_to_all_v(h.h, src.ptrs(), dst.ptrs(), [1 << 63] * 2 + [0] * 14, S) == P.PL_ERR_INVALID_ARG
+    assert P.purlin_reduce_scatter_v(h.h, src.ptrs(), dst.ptrs(), [1 << 63, 1 << 63, 4, 4], P.PL_F32, 0,
+                                     S) == P.PL_ERR_INVALID_ARG
     hh = h.h
     assert h.close() == P.PL_OK
     assert P.purlin_all_reduce(hh, src.ptrs(), dst.ptrs(), 64, P.PL_F32, 0, S) == P.PL_ERR_FINALIZED
