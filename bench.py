@@ -69,6 +69,13 @@ def workloads(P, inputs):
                  lambda: list(inputs.w2_allreduce_bf16(WORLD, N_ELEMS, seed=1)),
                  [S] * WORLD, lambda h, s, d, st: P.purlin_all_reduce(h, s, d, S, P.PL_BF16, 0, st),
                  ALGO_BYTES, P.PL_COLL_ALL_REDUCE, S, tune={"layout": P.PL_LAYOUT_TWO_SHOT}),
+        Workload("allreduce_ring_bf16_8x64MiB", WORKLOAD.replace("AllReduce sum", "AllReduce sum, ring layout "
+                 "(each chunk's partial sum passes rank to rank, rounded to bf16 at every hop, then the "
+                 "finished chunks pass around the ring: 2(N-1) SNAC stages per tile),", 1).replace(
+                 "fp32 ascending-rank accumulation", "fp32 adds in ring order"), "bf16",
+                 lambda: list(inputs.w2_allreduce_bf16(WORLD, N_ELEMS, seed=1)),
+                 [S] * WORLD, lambda h, s, d, st: P.purlin_all_reduce(h, s, d, S, P.PL_BF16, 0, st),
+                 ALGO_BYTES, P.PL_COLL_ALL_REDUCE, S, tune={"layout": P.PL_LAYOUT_RING}),
         Workload("reduce_scatter_f32_8x256MiB",
                  "ReduceScatter sum, 8 ranks, fp32, 64 Mi elements (256 MiB) per rank, U(-1,1), seed 2", "f32",
                  lambda: list(inputs.w3_reduce_scatter(WORLD, 64 * MI, seed=2, dtype="f32")),
@@ -522,7 +529,8 @@ def side_table(P, h, stream, dev):
         return d
 
     out = {"d2d_copy": {}, "all_gather_u8": {}, "all_to_all_u8": {}, "all_reduce_bf16": {},
-           "reduce_scatter_f32": {}, "all_reduce_two_shot_bf16": {}, "reduce_scatter_v_bf16": {},
+           "reduce_scatter_f32": {}, "all_reduce_two_shot_bf16": {}, "all_reduce_ring_bf16": {},
+           "reduce_scatter_v_bf16": {},
            "device_api_fused": {}, "atom_copy": {}, "atom_reduce": {}}
     chk = lambda st: P.check(st)
     for size in [1 << (10 + 2 * k) for k in range(10)]:          # 1 KiB .. 256 MiB per rank
@@ -550,9 +558,11 @@ def side_table(P, h, stream, dev):
         out["all_reduce_bf16"][key] = point(2 * WORLD * size, timeit(
             lambda: chk(P.purlin_all_reduce(h, x, y, size, P.PL_BF16, 0, stream))), size)
         if size >= 16 * MI:
-            P.check(P.purlin_tune_override(h, {"layout": P.PL_LAYOUT_TWO_SHOT}))
-            out["all_reduce_two_shot_bf16"][key] = point(2 * WORLD * size, timeit(
-                lambda: chk(P.purlin_all_reduce(h, x, y, size, P.PL_BF16, 0, stream))), size)
+            for layout, name in ((P.PL_LAYOUT_TWO_SHOT, "all_reduce_two_shot_bf16"),
+                                 (P.PL_LAYOUT_RING, "all_reduce_ring_bf16")):
+                P.check(P.purlin_tune_override(h, {"layout": layout}))
+                out[name][key] = point(2 * WORLD * size, timeit(
+                    lambda: chk(P.purlin_all_reduce(h, x, y, size, P.PL_BF16, 0, stream))), size)
             P.check(P.purlin_tune_override(h, None))
         del x, y
         x = bufs(size // 4, WORLD, torch.float32)
@@ -670,6 +680,7 @@ def _reference_call(name):
     return {
         "allreduce_bf16_8x64MiB": lambda ins: oracle.all_reduce(ins, "bf16"),
         "allreduce_two_shot_bf16_8x64MiB": lambda ins: oracle.all_reduce(ins, "bf16"),
+        "allreduce_ring_bf16_8x64MiB": lambda ins: oracle.all_reduce_ring(ins, "bf16"),
         "reduce_scatter_f32_8x256MiB": lambda ins: oracle.reduce_scatter(ins, "f32"),
         "reduce_scatter_bf16_8x128MiB": lambda ins: oracle.reduce_scatter(ins, "bf16"),
         "all_gather_u8_8x256MiB": oracle.all_gather,

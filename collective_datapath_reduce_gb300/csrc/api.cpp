@@ -105,6 +105,11 @@ const void* pick_kernel(const pl::Plan& p) {
     u = u >= 8 ? 8 : u >= 4 ? 4 : u >= 2 ? 2 : 1;
     return pl::kernel_copy(u);
   }
+  if (p.tune.layout == pl::kRing && p.sync) {
+    if (p.dtype == pl::kF32) return pl::kernel_reduce_ring_f32(p.tune.unroll);
+    if (p.dtype == pl::kBF16) return pl::kernel_reduce_ring_bf16(p.tune.unroll);
+    return nullptr;
+  }
   if (p.dtype == pl::kF32) return pl::kernel_reduce_f32(p.nsrc, p.tune.unroll);
   if (p.dtype == pl::kBF16) return pl::kernel_reduce_bf16(p.nsrc, p.tune.unroll);
   return nullptr;
@@ -456,11 +461,14 @@ extern "C" {
 
 size_t purlin_workspace_bytes(int world, size_t max_bytes_per_rank) {
   if (world < 1 || world > PURLIN_MAX_WORLD) return 0;
-  // two-shot AllReduce flags at the table's tile size, for the smallest element (bf16)
+  // flags of the SNAC AllReduce layouts at the table's tile size, for the
+  // smallest element (bf16): one per tile of each rank's share (two-shot), or
+  // one per tile and stage but the last of 2 (world - 1) stages (ring)
   const pl::Tune t = pl::tune_table(pl::kAllReduce, world, pl::kBF16, max_bytes_per_rank);
   const uint64_t per_owner = (max_bytes_per_rank / 2 + (uint64_t)world - 1) / (uint64_t)world * 2;
-  const uint64_t tiles = (per_owner + (uint64_t)t.chunk_bytes - 1) / (uint64_t)t.chunk_bytes;
-  return (size_t)pl::kCtlBytes + (size_t)(world * std::max<uint64_t>(tiles, 1)) * sizeof(uint32_t);
+  const uint64_t tiles = std::max<uint64_t>(1, (per_owner + (uint64_t)t.chunk_bytes - 1) / (uint64_t)t.chunk_bytes);
+  const uint64_t per_tile = world > 1 ? 2 * (uint64_t)world - 3 : 1;
+  return (size_t)pl::kCtlBytes + (size_t)((uint64_t)world * tiles * per_tile) * sizeof(uint32_t);
 }
 
 purlin_status purlin_initialize(int world, void* workspace, size_t workspace_bytes, purlin_stream_t stream,

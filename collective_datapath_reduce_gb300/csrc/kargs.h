@@ -56,6 +56,9 @@ static_assert(sizeof(TraceRecord) == 32, "trace record layout");
 const void* kernel_copy(int unroll);
 const void* kernel_reduce_f32(int nsrc, int unroll);
 const void* kernel_reduce_bf16(int nsrc, int unroll);
+// Ring AllReduce (reduce items that read partial sums stored in the same launch).
+const void* kernel_reduce_ring_f32(int unroll);
+const void* kernel_reduce_ring_bf16(int unroll);
 // TMA bulk pipeline variants (dynamic shared memory).
 const void* kernel_bulk_copy();
 const void* kernel_bulk_reduce_f32(int nsrc);

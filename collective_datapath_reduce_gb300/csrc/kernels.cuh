@@ -102,8 +102,11 @@ __device__ __forceinline__ void trace_put(const KArgs& a, unsigned long long t0,
 
 // T = void: copy-only kernel (AllGather, AllToAll and their V forms).
 // Otherwise items with one source are the consume-side copies of the
-// two-shot AllReduce, whose source another CTA produced in this launch.
-template <typename T, int NS, int U, bool STREAMING>
+// two-shot and ring AllReduce, whose source another CTA produced in this
+// launch.  COH: reduce items too may read data produced in this launch (the
+// ring's partial sums), so their loads go through the L2 rather than the
+// non-coherent read-only path.
+template <typename T, int NS, int U, bool STREAMING, bool COH>
 __device__ __forceinline__ void run_item(const char* const* src, int ns, char* const* dst, int nd,
                                          uint64_t len) {
   if constexpr (std::is_same<T, void>::value) {
@@ -112,7 +115,7 @@ __device__ __forceinline__ void run_item(const char* const* src, int ns, char* c
     if (ns == 1)
       copy_atom<true, 2, STREAMING>(src[0], dst, nd, len);
     else
-      reduce_atom<T, NS, U, STREAMING>(src, ns, dst, nd, len);
+      reduce_atom<T, NS, U, STREAMING, COH>(src, ns, dst, nd, len);
   }
 }
 
@@ -130,7 +133,7 @@ __device__ __forceinline__ void run_item(const char* const* src, int ns, char* c
 template <int NS>
 constexpr int snac_max_threads() { return NS == 0 ? 256 : 512; }
 
-template <typename T, int NS, int U>
+template <typename T, int NS, int U, bool COH = false>
 __global__ void __launch_bounds__(snac_max_threads<NS>(), 2) snac_kernel(const __grid_constant__ KArgs a) {
   constexpr uint32_t kNoItem = 0xFFFFFFFFu;
   __shared__ const char* s_src[kMaxWorld];
@@ -209,9 +212,9 @@ __global__ void __launch_bounds__(snac_max_threads<NS>(), 2) snac_kernel(const _
     const uint32_t i = s_item;
     if (i == kNoItem || !s_ok) break;
     if (a.store_hint == 2)
-      run_item<T, NS, U, true>(s_src, s_ns, s_dst, s_nd, s_len);
+      run_item<T, NS, U, true, COH>(s_src, s_ns, s_dst, s_nd, s_len);
     else
-      run_item<T, NS, U, false>(s_src, s_ns, s_dst, s_nd, s_len);
+      run_item<T, NS, U, false, COH>(s_src, s_ns, s_dst, s_nd, s_len);
     __syncthreads();
     if (threadIdx.x == 0) {
       if (s_notify && i + 1 != a.drop_notify) {

@@ -20,4 +20,10 @@ const void* kernel_reduce_bf16(int nsrc, int unroll) {
   }
 }
 
+// Ring AllReduce: two sources per reduce item, one of them a partial sum
+// another CTA stored in this launch (loads through the L2).
+const void* kernel_reduce_ring_bf16(int unroll) {
+  return unroll >= 2 ? (const void*)snac_kernel<bf16_tag, 2, 2, true> : (const void*)snac_kernel<bf16_tag, 2, 1, true>;
+}
+
 }  // namespace pl

@@ -293,19 +293,21 @@ Tune tune_merge(const Tune& b, const Tune& o) {
 
 Tune resolve_tune(int coll, int table_coll, int world, int dtype, uint64_t bytes_per_rank, const Tune& over) {
   Tune t = tune_merge(tune_table(table_coll, world, dtype, bytes_per_rank), over);
-  if (coll == kAllReduce && t.layout == kTwoShot) {
-    // the two-shot layout's own best (512 threads, two CTAs per SM, write-back
-    // stores, no grid cap) unless the caller set these fields
+  if (coll == kAllReduce && (t.layout == kTwoShot || t.layout == kRing)) {
+    // the SNAC layouts' own best (512 threads, two CTAs per SM, write-back
+    // stores, no grid cap) unless the caller set these fields; the ring's
+    // reduce items have two sources, so two vectors of each in flight
     if (!over.threads) t.threads = 512;
     if (!over.ctas_per_sm) t.ctas_per_sm = 2;
     if (!over.store_hint) t.store_hint = 1;
     if (!over.max_ctas) t.max_ctas = 0;
+    if (t.layout == kRing && !over.unroll) t.unroll = 2;
   }
   return t;
 }
 
 static int validate_tune(const Tune& t) {
-  if (t.layout < kOneShot || t.layout > kTwoShot) return PL_ERR_UNSUPPORTED;
+  if (t.layout < kOneShot || t.layout > kRing) return PL_ERR_UNSUPPORTED;
   if (t.threads < 64 || t.threads > 512 || t.threads % 32) return PL_ERR_INVALID_ARG;
   if (t.ctas_per_sm < 1 || t.ctas_per_sm > 32) return PL_ERR_INVALID_ARG;
   if (t.unroll < 1 || t.unroll > 8) return PL_ERR_INVALID_ARG;
@@ -411,6 +413,69 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
             for (int o = 0; o < world; ++o)
               if (t - lag < tiles[o]) copy_piece(o, t - lag);
         }
+      } else if (p.tune.layout == kRing && world > 1) {
+        // Ring (Iris docs, "Device Context", all_reduce_ring; the classic
+        // reduce-scatter then all-gather around the ranks).  The range is cut
+        // into `world` chunks and each chunk into tiles.  A tile passes
+        // through 2 (world - 1) stages, each waiting for the previous one's
+        // flag.  Reduce stage k = 1 .. world-1: rank r = j + k (mod world)
+        // folds its input with the partial sum of chunk j -- rank j's input
+        // for k = 1, else the output of rank r - 1 -- into its own output
+        // (rounded to the data type: the partial travels as a buffer of it).
+        // After stage world-1 rank j - 1 holds the finished chunk.  Gather
+        // stage m = 1 .. world-1: the output of rank j - 2 + m is copied to
+        // rank j - 1 + m.  Every output byte but those of ranks j - 1 and j is
+        // written twice, partial first, and the overwrite waits (through the
+        // chain) for the read of the partial.
+        if (p.tune.path != kPathRegister) return PL_ERR_UNSUPPORTED;  // the register-path kernel only
+        sync = true;
+        p.nsrc = 2;
+        const uint64_t n = S / E;
+        const uint64_t T = std::max<uint64_t>(16, (uint64_t)p.tune.chunk_bytes / 16 * 16);
+        uint64_t start[kMaxWorld + 1];
+        start[0] = 0;
+        for (int j = 0; j < world; ++j)
+          start[j + 1] = start[j] + (n / world + ((uint64_t)j < n % world ? 1 : 0)) * E;
+        uint64_t tiles[kMaxWorld], tmax = 0, n_items = 0;
+        const uint32_t stages = 2u * (uint32_t)world - 2u;
+        for (int j = 0; j < world; ++j) {
+          tiles[j] = ceil_div(start[j + 1] - start[j], T);
+          tmax = std::max(tmax, tiles[j]);
+          n_items += tiles[j] * stages;
+        }
+        // one flag per (chunk, tile, stage) except each tile's last stage
+        n_flags = (uint32_t)((uint64_t)world * tmax * (stages - 1));
+        auto flag = [&](int j, uint64_t t, uint32_t st) {
+          return (uint32_t)(((uint64_t)j * tmax + t) * (stages - 1) + st + 1);
+        };
+        const uint64_t gcap = (uint64_t)p.tune.ctas_per_sm * sm_count;
+        const uint64_t G = std::max<uint64_t>(1, std::min<uint64_t>(gcap, n_items));
+        // stage st of tile t is emitted `lag` tile steps after stage st - 1, so
+        // about one wave of CTAs separates a flag's notify from its wait
+        const uint64_t lag = std::max<uint64_t>(1, ceil_div(G, (uint64_t)world));
+        auto stage_piece = [&](int j, uint64_t t, uint32_t st) {
+          const uint64_t off = start[j] + t * T, len = std::min(T, start[j + 1] - off);
+          uint32_t src, dst;
+          if (st + 1 < (uint32_t)world) {
+            const int k = (int)st + 1, r = (j + k) % world, prev = (j + k - 1) % world;
+            src = (1u << r) | (k == 1 ? (1u << prev) : (1u << (16 + prev)));
+            dst = 1u << r;
+          } else {
+            const int m = (int)st - (world - 1) + 1;
+            src = 1u << (16 + (j - 2 + m + 2 * world) % world);
+            dst = 1u << ((j - 1 + m + world) % world);
+          }
+          Piece q{off, off, len, src, dst, st ? flag(j, t, st - 1) : 0u, st + 1 < stages ? flag(j, t, st) : 0u};
+          push_grouped(pieces, q, dst_res);
+        };
+        for (uint64_t step = 0; step < tmax + (uint64_t)(stages - 1) * lag; ++step)
+          for (uint32_t st = 0; st < stages; ++st) {
+            if (step < (uint64_t)st * lag) break;
+            const uint64_t t = step - (uint64_t)st * lag;
+            if (t >= tmax) continue;
+            for (int j = 0; j < world; ++j)
+              if (t < tiles[j]) stage_piece(j, t, st);
+          }
       } else {
         p.tune.layout = kOneShot;
         push_grouped(pieces, Piece{0, 0, S, ALL, ALL, 0, 0}, dst_res);
@@ -664,7 +729,13 @@ std::string check_plan(const Plan& p) {
       notified_at[it.notify - 1] = (int64_t)i;
     }
   }
-  std::vector<std::vector<std::pair<uint64_t, uint64_t>>> written(p.world);
+  // accesses to every output: {lo, hi, item, is_write}
+  struct Acc {
+    uint64_t lo, hi;
+    int64_t item;
+    bool write;
+  };
+  std::vector<std::vector<Acc>> acc(p.world);
   for (size_t i = 0; i < p.items.size(); ++i) {
     const Item& it = p.items[i];
     if (it.len == 0) return "empty item";
@@ -673,7 +744,9 @@ std::string check_plan(const Plan& p) {
     if (!it.dst_mask || (it.dst_mask & ~ALL)) return "destination mask empty or outside the world";
     const int nsrc = popcount32(it.src_mask);
     if (nsrc < 1) return "item without a source";
-    if (nsrc > 1 && out_bits) return "a reduce reads outputs";
+    // a reduce reads an output only in the ring layout (whose kernel loads
+    // such sources through the L2) and only after waiting for its producer
+    if (nsrc > 1 && out_bits && (p.tune.layout != kRing || !it.wait)) return "a reduce reads outputs";
     if (nsrc > 1 && ((it.src_off | it.dst_off | it.len) % (uint64_t)p.elem)) return "reduce not element aligned";
     for (uint32_t m = in_bits; m; m &= m - 1) {
       int r = __builtin_ctz(m);
@@ -685,6 +758,7 @@ std::string check_plan(const Plan& p) {
     for (uint32_t m = out_bits; m; m &= m - 1) {
       int r = __builtin_ctz(m);
       if (it.src_off + it.len > p.out_bytes[r]) return "reads past an output";
+      acc[r].push_back({it.src_off, it.src_off + it.len, (int64_t)i, false});
     }
     for (uint32_t m = it.dst_mask; m; m &= m - 1) {
       int r = __builtin_ctz(m);
@@ -692,7 +766,7 @@ std::string check_plan(const Plan& p) {
         err << "item " << i << " writes past output " << r;
         return err.str();
       }
-      written[r].push_back({it.dst_off, it.dst_off + it.len});
+      acc[r].push_back({it.dst_off, it.dst_off + it.len, (int64_t)i, true});
     }
     if (it.wait) {
       if (it.wait > (uint32_t)p.n_flags) return "wait flag out of range";
@@ -700,13 +774,41 @@ std::string check_plan(const Plan& p) {
       if (at < 0 || at >= (int64_t)i) return "wait without an earlier notify";
     }
   }
+  // item b comes after item a through a chain of waits: b waits for a flag
+  // that a, or an item after a in that sense, notified
+  auto chained = [&](int64_t a, int64_t b) {
+    for (int64_t k = b; k > a;) {
+      const uint32_t w = p.items[(size_t)k].wait;
+      if (!w) return false;
+      k = notified_at[w - 1];
+      if (k == a) return true;
+    }
+    return false;
+  };
   for (int r = 0; r < p.world; ++r) {
-    auto& w = written[r];
-    std::sort(w.begin(), w.end());
-    uint64_t covered = 0;
-    for (size_t k = 0; k < w.size(); ++k) {
-      if (k && w[k].first < w[k - 1].second) return "an output byte is written twice";
-      covered += w[k].second - w[k].first;
+    auto& v = acc[r];
+    std::sort(v.begin(), v.end(), [](const Acc& x, const Acc& y) {
+      return x.lo != y.lo ? x.lo < y.lo : x.hi != y.hi ? x.hi < y.hi : x.item < y.item;
+    });
+    uint64_t covered = 0, end_any = 0, end_write = 0;
+    for (size_t k = 0; k < v.size();) {
+      // one group: the accesses to one identical range, in item order
+      size_t e = k;
+      bool any_write = false;
+      while (e < v.size() && v[e].lo == v[k].lo && v[e].hi == v[k].hi) any_write |= v[e++].write;
+      if (v[k].lo < end_write || (any_write && v[k].lo < end_any))
+        return "an output byte is accessed under partly overlapping ranges, one of them written";
+      // every pair with a write must be ordered by a chain of waits
+      for (size_t x = k; x < e; ++x)
+        for (size_t y = x + 1; y < e; ++y)
+          if ((v[x].write || v[y].write) && v[x].item != v[y].item && !chained(v[x].item, v[y].item))
+            return v[x].write && v[y].write ? "an output byte is written twice" : "a read and a write of an output are not ordered";
+      if (any_write) {
+        covered += v[k].hi - v[k].lo;
+        end_write = std::max(end_write, v[k].hi);
+      }
+      end_any = std::max(end_any, v[k].hi);
+      k = e;
     }
     if (covered != p.out_bytes[r]) {
       err << "output " << r << " covered " << covered << " of " << p.out_bytes[r];

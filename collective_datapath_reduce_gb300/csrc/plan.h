@@ -36,7 +36,7 @@ enum Coll : int {
 
 enum Dtype : int { kU8 = 0, kF32 = 1, kBF16 = 2 };
 
-enum Layout : int { kLayoutAuto = 0, kOneShot = 1, kTwoShot = 2 };
+enum Layout : int { kLayoutAuto = 0, kOneShot = 1, kTwoShot = 2, kRing = 3 };
 
 enum Path : int { kPathRegister = 1, kPathBulk = 2 };
 
@@ -87,7 +87,7 @@ struct Plan {
   bool sync = false;         // items wait on / notify SNAC flags (CTAs must be co-resident)
   bool queue = false;        // CTAs take items from the shared queue (items in global order)
   int grid = 0;
-  int n_flags = 0;           // SNAC flags used (two-shot layout)
+  int n_flags = 0;           // SNAC flags used (two-shot and ring layouts)
   uint64_t in_bytes[kMaxWorld] = {};   // bytes each input must hold
   uint64_t out_bytes[kMaxWorld] = {};  // bytes each output must hold
   uint64_t work_bytes = 0;   // algorithmic bytes (each input byte read once, each output byte written once)
@@ -118,7 +118,9 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
                int max_ctas_per_sm, const Tune& tune, Plan* out);
 
 // Check a plan: every item inside the buffers it names, masks inside the
-// world, flags in range, each wait after its notify in global order.
+// world, flags in range, each wait after its notify in global order, every
+// output byte written, and two accesses to one output byte, one of them a
+// write, only on identical ranges linked by a chain of waits.
 // Returns an empty string when the plan is sound, else a description.
 std::string check_plan(const Plan& p);
 

@@ -95,14 +95,23 @@ typedef enum {
   PL_COLL_ATOM_REDUCE = 8
 } purlin_coll;
 
-/* AllReduce layouts (Iris docs, "Device Context", all_reduce_one_shot and
- * all_reduce_two_shot).  One-shot: every byte range is reduced once and the
- * sum stored to all ranks.  Two-shot: rank o reduces range o into its own
- * output and notifies; a consumer then copies that range to every other rank. */
+/* AllReduce layouts (Iris docs, "Device Context", all_reduce_one_shot,
+ * all_reduce_two_shot and all_reduce_ring).  One-shot: every byte range is
+ * reduced once and the sum stored to all ranks.  Two-shot: rank o reduces
+ * range o into its own output and notifies; a consumer then copies that range
+ * to every other rank.  Both give the ascending-rank fold described above.
+ * Ring: the classic ring -- chunk j's partial sum starts at rank j and each
+ * hop adds the next rank's elements and stores the partial, in the data
+ * type, to that rank's output; the finished chunks are then passed around
+ * the ring.  Its results are deterministic but differ from the ascending fold:
+ * each chunk is folded in its own rank order, and bf16 partials are rounded
+ * at every hop (for fp32 with two ranks they are the same).  Only on request;
+ * AUTO never picks it.  Register path only (PL_ERR_UNSUPPORTED otherwise). */
 typedef enum {
   PL_LAYOUT_AUTO = 0,
   PL_LAYOUT_ONE_SHOT = 1,
-  PL_LAYOUT_TWO_SHOT = 2
+  PL_LAYOUT_TWO_SHOT = 2,
+  PL_LAYOUT_RING = 3
 } purlin_layout;
 
 /* Tuning of one call (the role of Purlin's host tuning policies).  A zero field

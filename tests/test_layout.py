@@ -29,6 +29,10 @@ def _describe(coll, world, dtype, sizes, sres=None, dres=None, sm=152, tune=None
     return items, grid, nflags
 
 
+def popcount(m):
+    return bin(m).count("1")
+
+
 def _bytes(a):
     return np.ascontiguousarray(a).view(np.uint8).copy()
 
@@ -82,6 +86,60 @@ def test_all_reduce_plan(world, dtype, layout):
                         assert first_notify[it["wait"]] < i
                         # strided: a CTA runs its items in increasing global order
                         assert it["cta"] == i % grid
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 8, 16])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_ring_all_reduce_plan(world, dtype):
+    """The ring layout, run item by item on the host, gives the ring oracle's
+    result; its chains are ordered (every wait after its notify, each tile's
+    stages one after another), the overwrite of every partial sum waits for
+    the read of it, and the CTAs run their items in increasing global order."""
+    E = ESZ[dtype]
+    for n in (1, 7, 1000, 4096 + 3):
+        for sm in SMS:
+            ins = [_draw(dtype, n) for _ in range(world)]
+            sres = [int(x) * E % 16 for x in RNG.integers(0, 16, size=world)]
+            dres = [int(x) * E % 16 for x in RNG.integers(0, 16, size=world)]
+            tune = {"layout": P.PL_LAYOUT_RING, "chunk_bytes": 1024, "ctas_per_sm": 2}
+            items, grid, nflags = _describe(P.PL_COLL_ALL_REDUCE, world, DT[dtype], [n * E], sres, dres, sm, tune)
+            outs = [np.zeros(n * E, np.uint8) for _ in range(world)]
+            run_items(items, [_bytes(x) for x in ins], outs, dtype)
+            want = oracle.all_reduce_ring(ins, dtype)
+            for r in range(world):
+                assert np.array_equal(outs[r], _bytes(want[r])), (n, sm, r)
+            if world == 1:
+                continue
+            assert nflags > 0
+            notify_at = {}
+            for i, it in enumerate(items):
+                assert popcount(it["src_mask"]) in (1, 2) and popcount(it["dst_mask"]) == 1
+                if it["wait"]:
+                    assert it["wait"] in notify_at and notify_at[it["wait"]] < i
+                else:
+                    # a tile's first stage: reduce of two inputs
+                    assert it["src_mask"] >> 16 == 0 and popcount(it["src_mask"]) == 2
+                assert it["cta"] == i % grid
+                if it["notify"]:
+                    notify_at[it["notify"]] = i
+            stages = 2 * world - 2
+            tiles = sum(-(-b // 1024) for b in np.diff([x * E for x in oracle.ring_chunk_bounds(n, world)]))
+            assert len(items) == tiles * stages
+
+
+@pytest.mark.parametrize("world", [2, 4])
+def test_ring_plan_edge_cases(world):
+    # the ring runs on the register path only
+    st, *_ = P.purlin_plan_describe(P.PL_COLL_ALL_REDUCE, world, P.PL_BF16, [4096], None, None, 152,
+                                    {"layout": P.PL_LAYOUT_RING, "path": P.PATH_BULK})
+    assert st == P.PL_ERR_UNSUPPORTED
+    # fewer elements than ranks: empty chunks get no items, the others still complete
+    items, _, _ = _describe(P.PL_COLL_ALL_REDUCE, world, P.PL_F32, [4], tune={"layout": P.PL_LAYOUT_RING})
+    assert len(items) == 2 * world - 2
+    # the workspace the library sizes for a handle holds the ring's flags at the table's tile size
+    for S in (1 << 20, 64 << 20):
+        _, _, nflags = _describe(P.PL_COLL_ALL_REDUCE, world, P.PL_BF16, [S], tune={"layout": P.PL_LAYOUT_RING})
+        assert P.purlin_workspace_bytes(world, S) >= 256 + 4 * nflags
 
 
 @pytest.mark.parametrize("world", [1, 2, 5, 8])
