@@ -80,7 +80,8 @@ def test_checks_are_silent_on_correct_calls(checking, name, tune):
 @pytest.mark.parametrize("tune", [{"path": P.PATH_REGISTER},
                                   {"path": P.PATH_BULK},
                                   {"path": P.PATH_BULK, "schedule": P.PL_SCHED_QUEUE, "interleave_bytes": 8192},
-                                  {"path": P.PATH_REGISTER, "layout": P.PL_LAYOUT_TWO_SHOT, "chunk_bytes": 4096}])
+                                  {"path": P.PATH_REGISTER, "layout": P.PL_LAYOUT_TWO_SHOT, "chunk_bytes": 4096},
+                                  {"path": P.PATH_REGISTER, "layout": P.PL_LAYOUT_RING, "chunk_bytes": 4096}])
 def test_limited_output_is_caught(checking, tune):
     world = 4
     n = 4 * 40000
@@ -118,7 +119,8 @@ def test_limited_output_is_caught(checking, tune):
         P.check(P.purlin_all_reduce(h.h, src.ptrs(), dst.ptrs(), n * 2, P.PL_BF16, 0, stream()))
         sync()
         assert h.status() == 0
-        want = oracle.all_reduce(ins, "bf16")
+        ring = tune.get("layout") == P.PL_LAYOUT_RING
+        want = oracle.all_reduce_ring(ins, "bf16") if ring else oracle.all_reduce(ins, "bf16")
         for r in range(world):
             assert np.array_equal(dst.read(r, np.uint16), want[r])
     finally:

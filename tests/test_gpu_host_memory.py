@@ -181,3 +181,23 @@ def test_two_shot_on_pinned_host_buffers():
                 assert np.array_equal(dst[r].numpy().view(np.uint16), want[r])
     finally:
         assert h.close() == P.PL_OK
+
+
+def test_ring_on_pinned_host_buffers():
+    """The ring's partial sums live in host memory between hops (loads through the L2)."""
+    world, n = 4, (1 << 17) + 3
+    ins = [inputs.to_bf16_bits(RNG.standard_normal(n).astype(np.float32)) for _ in range(world)]
+    src = [pinned(x) for x in ins]
+    dst = [pinned_empty(n * 2) for _ in range(world)]
+    h = Handle(world)
+    try:
+        P.check(P.purlin_tune_override(h.h, {"layout": P.PL_LAYOUT_RING, "chunk_bytes": 16384}))
+        want = oracle.all_reduce_ring(ins, "bf16")
+        for _ in range(2):
+            P.check(P.purlin_all_reduce(h.h, src, dst, n * 2, P.PL_BF16, 0, stream()))
+            sync()
+            assert h.status() == 0
+            for r in range(world):
+                assert np.array_equal(dst[r].numpy().view(np.uint16), want[r])
+    finally:
+        assert h.close() == P.PL_OK

@@ -5,7 +5,7 @@ The layouts cut every piece into items of at most 1 GiB (the Atoms count
 each kind of kernel over buffers of 2.25 to 4.5 GiB per rank, with ragged
 sizes, in the default launch configuration:
 
-* AllReduce bf16, 2 ranks x 2.5 GiB (+6 bytes), one-shot and two-shot;
+* AllReduce bf16, 2 ranks x 2.5 GiB (+6 bytes), one-shot, two-shot and ring;
 * ReduceScatter fp32, 2 ranks x 2.5 GiB (bulk path, 1.25 GiB outputs);
 * AllGather u8, 2 ranks x 2.25 GiB (+5 bytes): outputs of 4.5 GiB, the second
   block at an odd offset;
@@ -95,7 +95,8 @@ def ar_inputs():
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("layout", [P.PL_LAYOUT_AUTO, P.PL_LAYOUT_TWO_SHOT])
+# (two ranks: the ring's sums equal the ascending fold, a + b = b + a)
+@pytest.mark.parametrize("layout", [P.PL_LAYOUT_AUTO, P.PL_LAYOUT_TWO_SHOT, P.PL_LAYOUT_RING])
 def test_all_reduce_2x2_5GiB(ar_inputs, layout):
     S, n, T, src = ar_inputs
     dst = RankBuffers([S] * 2)
