@@ -122,8 +122,9 @@ size_t n_sizes(int coll, int world) {
 //   AllToAll    from 16 MiB per rank the queue in 64 KiB parts, 5 slots (7096
 //               against 6864 item by item at 256 MiB, 6800 against 6557 at 64
 //               MiB); AllToAllV from 32 MiB the guided queue (parts
-//               shrinking to 64 KiB), 4 slots.  Below, register copies with
-//               streaming stores.
+//               shrinking to 64 KiB), 4 slots.  Below, register copies:
+//               write-back stores from 2 MiB (17-23% ahead of streaming
+//               stores at 2-8 MiB), streaming stores below.
 //   Copy Atom, one destination: from 32 MiB the queue in 64 KiB parts (6973
 //               against 6762 GB/s item by item at 1 GiB); from 4 MiB, 8
 //               vectors per thread.
@@ -258,6 +259,12 @@ Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
       } else {
         t.unroll = 2;
         t.store_hint = 2;
+        if (S >= 2 * MiB && coll == kAllToAll) {
+          // working sets of 32-256 MiB: write-back stores keep the outputs in
+          // the L2 (a CUDA graph of 10 calls after an L2-sized write: 12.2
+          // against 15.0 us at 4 MiB, 21.0 against 25.0 at 8 MiB)
+          t.store_hint = 1;
+        }
         if (S >= 1 * MiB) {
           t.threads = 512;
           t.min_cta_bytes = 32 * 1024;
