@@ -110,8 +110,8 @@ size_t n_sizes(int coll, int world) {
 //   ReduceScatter  from 64 MiB per rank the TMA bulk ring (2 slots x 32 KiB
 //               per source), above the copy bandwidth from 128 MiB (the
 //               traffic is 8 reads per write); below, the register path with
-//               3 CTAs of 256 threads per SM and evict-first stores (10%
-//               ahead of the ring at 16-32 MiB).
+//               3 CTAs of 256 threads per SM (10% ahead of the ring at 16-32
+//               MiB), write-back stores from 4 MiB.
 //   AllGather   from 8 MiB per rank the streamed bulk ring fed from the
 //               shared item queue in 16 KiB parts (6904 against 6466 GB/s for
 //               register copies at 8 x 256 MiB, 6361 against 5572 at 8 MiB);
@@ -127,7 +127,7 @@ size_t n_sizes(int coll, int world) {
 //               stores at 2-8 MiB), streaming stores below.
 //   Copy Atom, one destination: from 32 MiB the queue in 64 KiB parts (6973
 //               against 6762 GB/s item by item at 1 GiB); from 4 MiB, 8
-//               vectors per thread.
+//               vectors per thread, write-back stores.
 Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
   (void)dtype;
   const uint64_t S = bytes_per_rank;
@@ -181,9 +181,11 @@ Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
         t.chunk_bytes = 32 * 1024;
       } else {
         // register path, three CTAs per SM, evict-first stores (against the
-        // bulk ring: 6216 / 5567 GB/s at 8 x 16 MiB fp32, 6750 / 6163 at 32 MiB)
+        // bulk ring: 6216 / 5567 GB/s at 8 x 16 MiB fp32, 6750 / 6163 at 32 MiB);
+        // ReduceScatter from 4 MiB with write-back stores (a CUDA graph of 10
+        // calls after an L2-sized write: 3-6% ahead at 4-32 MiB, fp32 and bf16)
         t.ctas_per_sm = 3;
-        t.store_hint = 2;
+        t.store_hint = (coll == kReduceScatter && S >= 4 * MiB) ? 1 : 2;
       }
       break;
     case kAllGather:
@@ -199,10 +201,11 @@ Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
           t.schedule = kSchedQueue;
           t.interleave_bytes = 64 * 1024;
         } else {
+          // write-back stores: 5.01 against 5.27 us at 8 MiB (graph of 10 calls)
           t.threads = 512;
           t.unroll = 8;
           t.max_ctas = 128;
-          t.store_hint = 2;
+          t.store_hint = 1;
         }
       } else if (S >= 4 * MiB && coll == kAllGatherV) {
         // AllGatherV pieces are mostly misaligned: shifted bulk copies from
@@ -259,11 +262,13 @@ Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
       } else {
         t.unroll = 2;
         t.store_hint = 2;
-        if (S >= 2 * MiB && coll == kAllToAll) {
-          // working sets of 32-256 MiB: write-back stores keep the outputs in
+        if (S >= 1 * MiB && coll == kAllToAll) {
+          // working sets of 16-256 MiB: write-back stores keep the outputs in
           // the L2 (a CUDA graph of 10 calls after an L2-sized write: 12.2
-          // against 15.0 us at 4 MiB, 21.0 against 25.0 at 8 MiB)
+          // against 15.0 us at 4 MiB, 21.0 against 25.0 at 8 MiB; at 1 MiB
+          // with 4 vectors in flight, 4.96 against 6.22 us)
           t.store_hint = 1;
+          if (S < 2 * MiB) t.unroll = 4;
         }
         if (S >= 1 * MiB) {
           t.threads = 512;
