@@ -182,10 +182,11 @@ Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
       } else {
         // register path, three CTAs per SM, evict-first stores (against the
         // bulk ring: 6216 / 5567 GB/s at 8 x 16 MiB fp32, 6750 / 6163 at 32 MiB);
-        // ReduceScatter from 4 MiB with write-back stores (a CUDA graph of 10
-        // calls after an L2-sized write: 3-6% ahead at 4-32 MiB, fp32 and bf16)
+        // from 4 MiB with write-back stores (a CUDA graph of 10 calls after an
+        // L2-sized write: 3-6% ahead at 4-32 MiB, fp32 and bf16; 1-2% for the
+        // uneven chunks of ReduceScatterV at 36-40 MiB)
         t.ctas_per_sm = 3;
-        t.store_hint = (coll == kReduceScatter && S >= 4 * MiB) ? 1 : 2;
+        t.store_hint = S >= 4 * MiB ? 1 : 2;
       }
       break;
     case kAllGather:
