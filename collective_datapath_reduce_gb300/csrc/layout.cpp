@@ -315,6 +315,13 @@ Tune resolve_tune(int coll, int table_coll, int world, int dtype, uint64_t bytes
     if (!over.store_hint) t.store_hint = 1;
     if (!over.max_ctas) t.max_ctas = 0;
     if (t.layout == kRing && !over.unroll) t.unroll = 2;
+    if (t.layout == kRing && !over.chunk_bytes) {
+      // ring tiles of a 64th of a chunk, 64-128 KiB (graph of 10 calls, 8
+      // ranks: 64 KiB best at 16 MiB per rank, 95 against 129 us for 128 KiB;
+      // 128 KiB best at 64 MiB, 355 against 391 us for 64 KiB)
+      const uint64_t tile = bytes_per_rank / (uint64_t)std::max(world, 1) / 64 / 16 * 16;
+      t.chunk_bytes = (int)std::min<uint64_t>(128 * 1024, std::max<uint64_t>(64 * 1024, tile));
+    }
   }
   return t;
 }
