@@ -127,6 +127,18 @@ def test_ring_all_reduce_plan(world, dtype):
             assert len(items) == tiles * stages
 
 
+def test_ring_tiles_follow_the_chunk_size():
+    """Ring tiles are a 64th of a chunk, between 64 and 128 KiB, unless the caller sets chunk_bytes."""
+    MI = 1 << 20
+    for world, S, tile in ((8, 1 * MI, 65536), (8, 16 * MI, 65536), (8, 48 * MI, 98304), (8, 64 * MI, 131072),
+                           (8, 256 * MI, 131072), (16, 64 * MI, 65536), (2, 16 * MI, 131072)):
+        items, _, _ = _describe(P.PL_COLL_ALL_REDUCE, world, P.PL_BF16, [S], tune={"layout": P.PL_LAYOUT_RING})
+        assert max(int(it["len"]) for it in items) == min(tile, S // world), (world, S)
+    items, _, _ = _describe(P.PL_COLL_ALL_REDUCE, 8, P.PL_BF16, [64 * MI],
+                            tune={"layout": P.PL_LAYOUT_RING, "chunk_bytes": 32768})
+    assert max(int(it["len"]) for it in items) == 32768
+
+
 @pytest.mark.parametrize("world", [2, 4])
 def test_ring_plan_edge_cases(world):
     # the ring runs on the register path only
