@@ -117,12 +117,13 @@ size_t n_sizes(int coll, int world) {
 //               register copies at 8 x 256 MiB, 6361 against 5572 at 8 MiB);
 //               from 4 MiB register copies on 128 CTAs of 512 threads with
 //               evict-first stores (5756 against 5646 at 4 MiB).  AllGatherV
-//               (misaligned pieces): the queue in 32 KiB parts on 128 CTAs
-//               (5889 against 5681 item by item).
+//               (misaligned pieces): the guided queue on 128 CTAs, parts of
+//               32 KiB shrinking to 8 KiB (5889 against 5681 item by item for
+//               equal 32 KiB parts; the guided parts 1% faster again).
 //   AllToAll    from 16 MiB per rank the queue in 64 KiB parts, 5 slots (7096
 //               against 6864 item by item at 256 MiB, 6800 against 6557 at 64
-//               MiB); AllToAllV from 32 MiB the guided queue (parts
-//               shrinking to 64 KiB), 4 slots.  Below, register copies:
+//               MiB); AllToAllV from 32 MiB the guided queue (parts of
+//               256 KiB shrinking to 64 KiB), 4 slots.  Below, register copies:
 //               write-back stores from 2 MiB (17-23% ahead of streaming
 //               stores at 2-8 MiB), streaming stores below.
 //   Copy Atom, one destination: from 32 MiB the queue in 64 KiB parts (6973
@@ -210,14 +211,15 @@ Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
         }
       } else if (S >= 4 * MiB && coll == kAllGatherV) {
         // AllGatherV pieces are mostly misaligned: shifted bulk copies from
-        // the shared queue in 32 KiB parts, 128 CTAs
+        // the guided queue (parts of 32 KiB shrinking to 8 KiB at the end:
+        // 66.0 against 66.7 us for equal 32 KiB parts), 128 CTAs
         t.path = kPathBulk;
         t.ctas_per_sm = 1;
         t.max_ctas = 128;
         t.stages = 3;
         t.chunk_bytes = 32 * 1024;
-        t.schedule = kSchedQueue;
-        t.interleave_bytes = 32 * 1024;
+        t.schedule = kSchedQueueGuided;
+        t.interleave_bytes = 8 * 1024;
       } else if (S >= 8 * MiB && coll == kAllGather) {
         // one bulk load, `world` bulk stores per chunk, one CTA per SM, parts
         // from the shared queue: 16 KiB with 3 slots for 8 ranks, 64 KiB with
@@ -660,13 +662,15 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
     // part ends in the concatenated piece space (the last one is W)
     std::vector<uint64_t> ends;
     if (p.tune.schedule == kSchedQueueGuided) {
-      // guided: each part is 1/(2 grid) of what is left, down to
-      // interleave_bytes: large parts first (few items), small ones last
-      // (the CTAs that run slower stop at nearly the same time)
+      // guided: each part is 1/(2 grid) of what is left, between
+      // interleave_bytes and four times that: larger parts first (fewer
+      // items), small ones last (the CTAs that run slower stop at nearly the
+      // same time).  The cap keeps the CTAs' first parts close together in
+      // the buffers (AllToAllV workload: 86.8 against 88.9 us uncapped)
       const uint64_t T = p.tune.interleave_bytes > 0 ? (uint64_t)p.tune.interleave_bytes : kQueuePartBytes;
       uint64_t pos = 0;
       while (pos < W) {
-        uint64_t part = std::max<uint64_t>(T, (W - pos) / (2 * G));
+        uint64_t part = std::max<uint64_t>(T, std::min<uint64_t>(4 * T, (W - pos) / (2 * G)));
         part = (part + kSplitGranule - 1) & ~(kSplitGranule - 1);
         pos = (W - pos <= part) ? W : pos + part;
         ends.push_back(pos);

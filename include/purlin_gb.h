@@ -144,10 +144,11 @@ typedef struct {
  * path (path = 1; two-shot SNAC plans included: an item only waits on
  * earlier items, so the earliest unfinished item always runs) and copy
  * collectives on the bulk path.  QUEUE_GUIDED is the queue with parts that
- * shrink as the work runs out: each is 1/(2 x grid) of what is left, down to
- * interleave_bytes (else 256 KiB), so the first parts are large (few items)
- * and the last ones small (CTAs that run slower finish at nearly the same
- * time).  Other combinations return PL_ERR_UNSUPPORTED. */
+ * shrink as the work runs out: each is 1/(2 x grid) of what is left, kept
+ * between T and 4 T bytes (T = interleave_bytes, else 256 KiB), so the
+ * first parts are larger (fewer items) and the last ones small (CTAs that
+ * run slower finish at nearly the same time).  Other combinations return
+ * PL_ERR_UNSUPPORTED. */
 typedef enum { PL_SCHED_ITEM = 1, PL_SCHED_STREAM = 2, PL_SCHED_QUEUE = 3, PL_SCHED_QUEUE_GUIDED = 4 } purlin_schedule;
 
 /* One work item of a plan, as purlin_plan_describe reports it. */
