@@ -9,6 +9,11 @@
 //       rank o owns the o-th of world near-equal element ranges; per tile t of
 //       that range a reduce piece writes out[o] and raises flag (o, t), and a
 //       copy piece waits on the flag and copies out[o] to every other output.
+//   AllReduce, ring  (same page, all_reduce_ring, read as the classic ring):
+//       per tile of chunk j, 2 (world - 1) stages chained by flags: world - 1
+//       reduce pieces of two sources (the next rank's input and the partial
+//       sum the previous stage left in the previous rank's output), then
+//       world - 1 copies that pass the finished tile around the ring.
 //   ReduceScatter  (NKI, reduce_scatter_hbm_kernel): piece r reduces chunk r of
 //       all inputs into out[r].
 //   AllGather      (NKI, all_gather_hbm_kernel): piece s copies in[s] to offset
