@@ -367,6 +367,7 @@ purlin_status run(purlin_ctx* h, int coll, int world, int dtype, const uint64_t*
   a.chunk_bytes = d->ring_chunk;
   a.trace = h->trace;
   a.trace_cap = h->trace_cap;
+  a.flag_cap = (uint32_t)std::min<size_t>(h->flag_cap, 0xFFFFFFFFu);
   h->drop_notify = -1;
   for (int r = 0; r < pl::kMaxWorld; ++r) {
     a.in_bytes[r] = d->plan.in_bytes[r];
@@ -778,6 +779,16 @@ purlin_status purlin_debug_drop_notify(purlin_handle h, long long item) {
   std::lock_guard<std::mutex> lock(h->mu);
   h->drop_notify = item < 0 ? -1 : item;
   return PL_OK;
+}
+
+purlin_status purlin_debug_set_epoch(purlin_handle h, uint32_t epoch, purlin_stream_t stream) {
+  purlin_status st;
+  if ((st = check_handle(h))) return st;
+  std::lock_guard<std::mutex> lock(h->mu);
+  cudaError_t e = cudaMemcpyAsync(h->ctl + pl::kCtlEpoch, &epoch, sizeof epoch, cudaMemcpyHostToDevice,
+                                  (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);  // `epoch` is on this stack
+  return cuda_fail(e);
 }
 
 purlin_status purlin_debug_limit_buffer(purlin_handle h, int is_output, int rank, uint64_t bytes) {

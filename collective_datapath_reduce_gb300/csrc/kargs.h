@@ -37,6 +37,7 @@ struct KArgs {
   uint32_t trace_cap;         // records the trace buffer holds
   uint64_t in_bytes[kMaxWorld];   // bytes of each input and output buffer (the
   uint64_t out_bytes[kMaxWorld];  // checking build tests every item against them)
+  uint32_t flag_cap;              // flags the workspace holds (cleared when the epoch wraps)
 };
 
 // One trace record (32 bytes): which CTA ran which item, when, and how long it

@@ -53,6 +53,36 @@ __device__ __forceinline__ bool consume_wait(const KArgs& a, const uint32_t* fla
   }
 }
 
+// End of a launch of a plan with SNAC flags; every thread of every CTA calls
+// it once its items are done.  The last CTA to get here publishes the
+// launch's epoch for the next launch (and resets the shared queue).  Epochs
+// run 1, 2, ..., 0xFFFFFFFF and start again at 1: the launch that used
+// 0xFFFFFFFF clears every flag of the workspace and publishes 0, so a flag
+// written in one cycle can never equal an epoch of the next (flags start at
+// 0, and no launch uses epoch 0).
+__device__ __forceinline__ void snac_finish(const KArgs& a, uint32_t epoch, bool reset_queue) {
+  __shared__ int s_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(&a.ctl[kCtlDone], 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  const bool wrap = epoch == 0xFFFFFFFFu;
+  if (wrap) {
+    for (uint32_t i = threadIdx.x; i < a.flag_cap; i += blockDim.x) a.flags[i] = 0u;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    a.ctl[kCtlDone] = 0u;
+    a.ctl[kCtlEpoch] = wrap ? 0u : epoch;
+    if (reset_queue) a.ctl[kCtlQueue] = 0u;
+    __threadfence();
+  }
+}
+
 // Programmatic dependent launch.  The library launches its kernels with
 // programmatic stream serialization, so a launch may start as soon as the
 // previous kernel on the stream has retired its CTAs, without waiting for
@@ -225,20 +255,8 @@ __global__ void __launch_bounds__(snac_max_threads<NS>(), 2) snac_kernel(const _
     }
   }
   if (a.sync) {
-    // The last CTA to finish publishes the launch's epoch for the next one
-    // (and resets the queue: every CTA made its last fetch before counting
-    // itself done).
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      __threadfence();
-      const uint32_t done = atomicAdd(&a.ctl[kCtlDone], 1u);
-      if (done == gridDim.x - 1) {
-        a.ctl[kCtlDone] = 0u;
-        a.ctl[kCtlEpoch] = s_epoch;
-        if (a.queue) a.ctl[kCtlQueue] = 0u;
-        __threadfence();
-      }
-    }
+    // (every CTA made its last queue fetch before counting itself done)
+    snac_finish(a, s_epoch, a.queue != 0);
   } else if (a.queue) {
     __syncthreads();
     if (threadIdx.x == 0) {

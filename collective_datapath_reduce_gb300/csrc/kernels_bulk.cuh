@@ -474,18 +474,7 @@ __global__ void __launch_bounds__(512, 1) bulk_kernel(const __grid_constant__ KA
     }
   }
   if (threadIdx.x == 0) bulk_wait_all();  // shared memory stays valid until every store has read it
-  if (a.sync) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      __threadfence();
-      const uint32_t done = atomicAdd(&a.ctl[kCtlDone], 1u);
-      if (done == gridDim.x - 1) {
-        a.ctl[kCtlDone] = 0u;
-        a.ctl[kCtlEpoch] = s_epoch;
-        __threadfence();
-      }
-    }
-  }
+  if (a.sync) snac_finish(a, s_epoch, false);
 }
 
 }  // namespace pl

@@ -12,7 +12,8 @@
 // The array lives in every GPU that loads the library until the process
 // exits.  Every call on a device shares it and it keeps the last call's
 // contents; flags carry the launch's epoch, so stale values never match and
-// nothing has to be cleared between calls.  Calls that overlap on the GPU
+// nothing has to be cleared between calls (except once every 2^32 - 1 calls,
+// when the epoch wraps and the last launch of the cycle clears the flags).  Calls that overlap on the GPU
 // (different streams, no ordering) race on the array and must not be made.
 #include <cuda_runtime.h>
 
@@ -135,17 +136,31 @@ __global__ void __launch_bounds__(kNaThreads, 2) noalloc_kernel(const __grid_con
       st_release(a.scratch + kNaCtlWords + s_flag, s_epoch);
     }
   }
+  // The last CTA publishes the epoch.  Epochs run 1 .. 0xFFFFFFFF and start
+  // again at 1: the launch that used 0xFFFFFFFF clears the flags and the
+  // failure word and publishes 0, so no value of one cycle matches the next.
+  __shared__ int s_last;
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    const uint32_t done = atomicAdd(a.scratch + kNaDone, 1u);
-    if (done == gridDim.x - 1) {
-      a.scratch[kNaDone] = 0u;
-      a.scratch[kNaEpoch] = s_epoch;
-      if (a.device_status)
-        *a.device_status = ld_volatile(a.scratch + kNaFailed) == s_epoch ? (int)PL_ERR_TIMEOUT : (int)PL_OK;
-      __threadfence();
-    }
+    s_last = atomicAdd(a.scratch + kNaDone, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  const bool wrap = s_epoch == 0xFFFFFFFFu;
+  if (threadIdx.x == 0 && a.device_status)
+    *a.device_status = ld_volatile(a.scratch + kNaFailed) == s_epoch ? (int)PL_ERR_TIMEOUT : (int)PL_OK;
+  __syncthreads();
+  if (wrap) {
+    for (uint32_t i = threadIdx.x; i < (uint32_t)kNaMaxFlags; i += blockDim.x) a.scratch[kNaCtlWords + i] = 0u;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    a.scratch[kNaDone] = 0u;
+    if (wrap) a.scratch[kNaFailed] = 0u;
+    a.scratch[kNaEpoch] = wrap ? 0u : s_epoch;
+    __threadfence();
   }
 }
 
@@ -192,6 +207,25 @@ purlin_status na_setup(int dev, cudaStream_t stream, NaDevice* out) {
 
 }  // namespace
 }  // namespace pl
+
+extern "C" purlin_status purlin_debug_noalloc_set_epoch(uint32_t epoch, purlin_stream_t stream) {
+  using namespace pl;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNaMaxDevices) {
+    (void)cudaGetLastError();
+    return PL_ERR_CUDA;
+  }
+  NaDevice d;
+  if (purlin_status st = na_setup(dev, (cudaStream_t)stream, &d)) return st;
+  cudaError_t e = cudaMemcpyAsync(d.scratch + kNaEpoch, &epoch, sizeof epoch, cudaMemcpyHostToDevice,
+                                  (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);  // `epoch` is on this stack
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return PL_ERR_CUDA;
+  }
+  return PL_OK;
+}
 
 extern "C" purlin_status purlin_all_reduce_noalloc(int world, const void* const* src, void* const* dst,
                                                    size_t bytes_per_rank, purlin_dtype dtype, int* device_status,

@@ -93,6 +93,8 @@ _SIGNATURES = {
     "purlin_tune_override": (_i, [_vp, ctypes.POINTER(purlin_tune)]),
     "purlin_set_wait_timeout_ns": (_i, [_vp, ctypes.c_uint64]),
     "purlin_debug_limit_buffer": (_i, [_vp, _i, _i, ctypes.c_uint64]),
+    "purlin_debug_set_epoch": (_i, [_vp, ctypes.c_uint32, _vp]),
+    "purlin_debug_noalloc_set_epoch": (_i, [ctypes.c_uint32, _vp]),
     "purlin_debug_drop_notify": (_i, [_vp, ctypes.c_longlong]),
     "purlin_query": (_i, [_vp, ctypes.POINTER(_i), ctypes.POINTER(_i), ctypes.POINTER(_i)]),
     "purlin_all_reduce_noalloc": (_i, [_i, _PP, _PP, _sz, _i, _vp, _vp]),
@@ -301,6 +303,14 @@ def purlin_debug_drop_notify(h, item: int) -> int:
 
 def purlin_debug_limit_buffer(h, is_output: int, rank: int, nbytes: int) -> int:
     return load().purlin_debug_limit_buffer(h, int(is_output), int(rank), int(nbytes))
+
+
+def purlin_debug_set_epoch(h, epoch: int, stream=None) -> int:
+    return load().purlin_debug_set_epoch(h, int(epoch), _stream(stream))
+
+
+def purlin_debug_noalloc_set_epoch(epoch: int, stream=None) -> int:
+    return load().purlin_debug_noalloc_set_epoch(int(epoch), _stream(stream))
 
 
 def purlin_trace_enable(h, buffer=None, buffer_bytes: int = 0) -> int:

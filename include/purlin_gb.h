@@ -284,6 +284,17 @@ purlin_status purlin_tune_override(purlin_handle h, const purlin_tune* t);
  * has no effect (there is no check to fire). */
 purlin_status purlin_debug_limit_buffer(purlin_handle h, int is_output, int rank, uint64_t bytes);
 
+/* Test hook: set the SNAC epoch counter of the handle (the epoch the last
+ * launch with SNAC flags used), in stream order.  Launches of SNAC plans use
+ * epochs 1 .. 0xFFFFFFFF, one per launch, and flags are ready when they hold
+ * the launch's epoch; the launch that used 0xFFFFFFFF clears every flag and
+ * the counter starts again at 1.  Setting the counter near the end of the
+ * cycle lets a test run that wrap without 2^32 launches. */
+purlin_status purlin_debug_set_epoch(purlin_handle h, uint32_t epoch, purlin_stream_t stream);
+
+/* The same for purlin_all_reduce_noalloc's scratch on the current device. */
+purlin_status purlin_debug_noalloc_set_epoch(uint32_t epoch, purlin_stream_t stream);
+
 /* Time limit of every SNAC consume wait, in nanoseconds (default 2e9). */
 purlin_status purlin_set_wait_timeout_ns(purlin_handle h, uint64_t ns);
 

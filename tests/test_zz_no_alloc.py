@@ -70,3 +70,29 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     assert P.purlin_all_reduce_noalloc(world, fake_src, fake_dst, S, P.PL_BF16, None, stream()) == P.PL_ERR_WORKSPACE
     assert P.purlin_all_reduce_noalloc(world, fake_src, fake_dst, 64 << 10, P.PL_U8, None, stream()) == \
         P.PL_ERR_UNSUPPORTED
+
+
+def test_noalloc_across_the_epoch_wrap():
+    """The scratch's epoch counter set near the end of its cycle: calls before,
+    at and after the wrap all give the handle-based AllReduce's result."""
+    world, n, dtype = 8, (1 << 18) + 3, "bf16"
+    rng = np.random.default_rng(7)
+    src = RankBuffers([n * 2] * world)
+    ref = RankBuffers([n * 2] * world)
+    out = RankBuffers([n * 2] * world)
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda:0")
+    h = Handle(world)
+    try:
+        P.check(P.purlin_debug_noalloc_set_epoch(0xFFFFFFFD, stream()))
+        for call in range(4):
+            src.upload([_draw(rng, dtype, n) for _ in range(world)])
+            out.fill(0)
+            status.fill_(-1)
+            P.check(P.purlin_all_reduce(h.h, src.ptrs(), ref.ptrs(), n * 2, P.PL_BF16, 0, stream()))
+            P.check(P.purlin_all_reduce_noalloc(world, src.ptrs(), out.ptrs(), n * 2, P.PL_BF16, status, stream()))
+            sync()
+            assert int(status.item()) == P.PL_OK, call
+            for r in range(world):
+                assert np.array_equal(out.read(r, np.uint16), ref.read(r, np.uint16)), (call, r)
+    finally:
+        assert h.close() == P.PL_OK
