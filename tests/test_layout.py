@@ -2,9 +2,10 @@
 
 Covers every collective, worlds 1..16, sizes with ragged tails, unaligned
 V counts, buffer addresses with mixed residues modulo 16, tiny grids (many
-items per CTA) and big grids (many CTAs per piece), and both AllReduce
-layouts.  Also checks the plan's bookkeeping: CTA assignment and the SNAC
-rule that every wait follows its notify in global order.
+items per CTA) and big grids (many CTAs per piece), and the three AllReduce
+layouts (the ring against the ring oracle).  Also checks the plan's
+bookkeeping: CTA assignment and the SNAC rule that every wait follows its
+notify in global order.
 """
 
 import numpy as np
