@@ -784,6 +784,7 @@ purlin_status purlin_debug_drop_notify(purlin_handle h, long long item) {
 purlin_status purlin_debug_set_epoch(purlin_handle h, uint32_t epoch, purlin_stream_t stream) {
   purlin_status st;
   if ((st = check_handle(h))) return st;
+  if (capturing((cudaStream_t)stream)) return PL_ERR_INVALID_ARG;  // a captured copy would read a dead stack slot
   std::lock_guard<std::mutex> lock(h->mu);
   cudaError_t e = cudaMemcpyAsync(h->ctl + pl::kCtlEpoch, &epoch, sizeof epoch, cudaMemcpyHostToDevice,
                                   (cudaStream_t)stream);

@@ -215,6 +215,11 @@ extern "C" purlin_status purlin_debug_noalloc_set_epoch(uint32_t epoch, purlin_s
     (void)cudaGetLastError();
     return PL_ERR_CUDA;
   }
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing((cudaStream_t)stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+    (void)cudaGetLastError();
+    return PL_ERR_INVALID_ARG;  // a captured copy would read a dead stack slot
+  }
   NaDevice d;
   if (purlin_status st = na_setup(dev, (cudaStream_t)stream, &d)) return st;
   cudaError_t e = cudaMemcpyAsync(d.scratch + kNaEpoch, &epoch, sizeof epoch, cudaMemcpyHostToDevice,

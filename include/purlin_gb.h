@@ -289,7 +289,8 @@ purlin_status purlin_debug_limit_buffer(purlin_handle h, int is_output, int rank
  * epochs 1 .. 0xFFFFFFFF, one per launch, and flags are ready when they hold
  * the launch's epoch; the launch that used 0xFFFFFFFF clears every flag and
  * the counter starts again at 1.  Setting the counter near the end of the
- * cycle lets a test run that wrap without 2^32 launches. */
+ * cycle lets a test run that wrap without 2^32 launches.  Waits for the
+ * stream; refused (PL_ERR_INVALID_ARG) while the stream is being captured. */
 purlin_status purlin_debug_set_epoch(purlin_handle h, uint32_t epoch, purlin_stream_t stream);
 
 /* The same for purlin_all_reduce_noalloc's scratch on the current device. */
