@@ -122,7 +122,8 @@ typedef struct {
   int threads;      /* threads per CTA: a multiple of 32 in [64, 512] */
   int unroll;       /* 16-byte vectors in flight per thread per source, 1..8 */
   int path;         /* 1 = register path, 2 = TMA bulk pipeline through shared memory */
-  int chunk_bytes;  /* TMA stage size per source, or SNAC tile size for the two-shot layout */
+  int chunk_bytes;  /* TMA stage size per source, or SNAC tile size of the two-shot and ring
+                       layouts (ring default: a 64th of a chunk, 64-128 KiB) */
   int stages;       /* TMA pipeline depth, 2..8 */
   int store_hint;   /* 1 = default write-back stores, 2 = streaming (evict-first) stores */
   int min_cta_bytes;/* fewest work bytes given to one CTA before the grid shrinks */
@@ -190,9 +191,10 @@ purlin_status purlin_finalize(purlin_handle h, purlin_stream_t stream);
 /* ----------------------------------------------------------- collectives */
 
 /* AllReduce (NKI all_reduce_hbm_kernel: sum tensors across ranks): dst[r][i] =
- * sum over s of src[s][i] for every r.  bytes_per_rank = size of each input
- * and each output.  dtype PL_F32 or PL_BF16.  In-place (src[r] == dst[r]) is
- * allowed. */
+ * sum over s of src[s][i] for every r, folded as described at the top (the
+ * ring layout folds in its own order; see purlin_layout).  bytes_per_rank =
+ * size of each input and each output.  dtype PL_F32 or PL_BF16.  In-place
+ * (src[r] == dst[r]) is allowed. */
 purlin_status purlin_all_reduce(purlin_handle h, const void* const* src, void* const* dst,
                                 size_t bytes_per_rank, purlin_dtype dtype, purlin_mode mode,
                                 purlin_stream_t stream);
@@ -264,8 +266,8 @@ purlin_status purlin_status_get(purlin_handle h, purlin_stream_t stream, int* de
 const char* purlin_status_string(purlin_status s);
 
 /* The tuning the handle would use for a call: table entry, then the
- * handle's override, then the layout's own defaults (two-shot AllReduce) and
- * the thread cap of the register path beyond 8 sources. */
+ * handle's override, then the layout's own defaults (two-shot and ring
+ * AllReduce) and the thread cap of the register path beyond 8 sources. */
 purlin_status purlin_tune_get(purlin_handle h, purlin_coll coll, purlin_dtype dtype,
                               size_t bytes_per_rank, purlin_tune* out);
 
