@@ -1,6 +1,6 @@
 """SNAC schedules run on the CPU with one thread per CTA (no GPU).
 
-The two-shot AllReduce plan deals its items round-robin to the CTAs; each
+The two-shot and ring AllReduce plans deal their items round-robin to the CTAs; each
 item that consumes a flag waits (bounded) until the item that notifies it has
 run.  Here every CTA is a Python thread that walks its items in the kernel's
 order, waits on flags set by other threads, and applies the item to host
@@ -53,19 +53,25 @@ def run_threads(items, grid, ins, outs, dtype, drop=None, timeout=5.0):
     return not status["failed"]
 
 
+LAYOUTS = [(P.PL_LAYOUT_TWO_SHOT, oracle.all_reduce), (P.PL_LAYOUT_RING, oracle.all_reduce_ring)]
+
+
 @pytest.mark.parametrize("sm", [1, 3, 16])
 @pytest.mark.parametrize("world", [2, 3, 8])
-def test_two_shot_schedule_completes_under_threads(sm, world):
+@pytest.mark.parametrize("layout,ref", LAYOUTS, ids=["two_shot", "ring"])
+def test_snac_schedule_completes_under_threads(sm, world, layout, ref):
+    """Two-shot: one wait per copy.  Ring: a chain of 2 (world - 1) stages per
+    tile, whose partial sums are overwritten later in the same chain."""
     rng = np.random.default_rng(world * 100 + sm)
     n = 5000 * world + 3
     ins = [oracle.f32_to_bf16_rne(rng.standard_normal(n).astype(np.float32)) for _ in range(world)]
-    tune = {"layout": P.PL_LAYOUT_TWO_SHOT, "chunk_bytes": 1024, "ctas_per_sm": 2}
+    tune = {"layout": layout, "chunk_bytes": 1024, "ctas_per_sm": 2}
     st, items, grid, nflags = P.purlin_plan_describe(P.PL_COLL_ALL_REDUCE, world, P.PL_BF16, [n * 2], None, None,
                                                      sm, tune)
     assert st == P.PL_OK and nflags > 0
     outs = [np.zeros(n * 2, np.uint8) for _ in range(world)]
     assert run_threads(items, grid, [x.view(np.uint8).copy() for x in ins], outs, "bf16")
-    want = oracle.all_reduce(ins, "bf16")
+    want = ref(ins, "bf16")
     for r in range(world):
         assert np.array_equal(outs[r].view(np.uint16), want[r])
 
