@@ -104,7 +104,7 @@ __device__ __forceinline__ bool item_in_bounds(const KArgs& a, const Item& it) {
     const int b = __ffs(m) - 1;
     if (end > (b < 16 ? a.in_bytes[b] : a.out_bytes[b - 16])) return false;
   }
-  for (uint32_t m = it.dst_mask; m; m &= m - 1)
+  for (uint32_t m = it.dst_mask & kDstRanks; m; m &= m - 1)
     if (it.dst_off + it.len > a.out_bytes[__ffs(m) - 1]) return false;
   return true;
 #else
@@ -130,22 +130,149 @@ __device__ __forceinline__ void trace_put(const KArgs& a, unsigned long long t0,
   }
 }
 
+// --------------------------------------------------- ring stages on bf16
+
+// The ring AllReduce over bf16 data keeps its running sum in binary32, as two
+// 16-bit halves in two rank outputs (kSplitSrc / kSplitDst items; plan.h).
+// A stage adds one bf16 input to that sum (SS: sources are {input, low half,
+// high half}) or, at the first stage, adds two inputs (sources {a, b}), and
+// stores the new sum as halves (SD: destinations {low, high}) or, at the last
+// stage, rounds it once to bf16 (one destination).  The halves were stored
+// by another CTA earlier in the launch, so every load goes through the L2.
+
+// Element k of every buffer.
+template <bool SS, bool SD>
+__device__ __forceinline__ void ring_elem_bf16(const char* const* src, char* const* dst, uint64_t k) {
+  const uint64_t o = k * 2;
+  float s;
+  if (SS) {
+    const uint32_t lo = __ldcg(reinterpret_cast<const unsigned short*>(src[1] + o));
+    const uint32_t hi = __ldcg(reinterpret_cast<const unsigned short*>(src[2] + o));
+    s = __fadd_rn(__uint_as_float((hi << 16) | lo), Elem<bf16_tag>::load_l2(src[0] + o));
+  } else {
+    s = __fadd_rn(Elem<bf16_tag>::load_l2(src[0] + o), Elem<bf16_tag>::load_l2(src[1] + o));
+  }
+  if (SD) {
+    const uint32_t b = __float_as_uint(s);
+    *reinterpret_cast<unsigned short*>(dst[0] + o) = (unsigned short)(b & 0xFFFFu);
+    *reinterpret_cast<unsigned short*>(dst[1] + o) = (unsigned short)(b >> 16);
+  } else {
+    Elem<bf16_tag>::store(dst[0] + o, s);
+  }
+}
+
+// Two elements held in one 32-bit word of each operand.  x: the bf16 input
+// pair (or the first input pair); y / z: the low and high half words of the
+// running sums (or, without SS, the second input pair).  Result: the words
+// to store, the low and high halves of the new sums (SD), or the pair
+// rounded to bf16 in `lo`.
+template <bool SS, bool SD>
+__device__ __forceinline__ void ring_word(uint32_t x, uint32_t y, uint32_t z, uint32_t& lo, uint32_t& hi) {
+  const float x0 = __uint_as_float(x << 16), x1 = __uint_as_float(x & 0xFFFF0000u);
+  float s0, s1;
+  if (SS) {
+    s0 = __fadd_rn(__uint_as_float(__byte_perm(y, z, 0x5410)), x0);
+    s1 = __fadd_rn(__uint_as_float(__byte_perm(y, z, 0x7632)), x1);
+  } else {
+    s0 = __fadd_rn(x0, __uint_as_float(y << 16));
+    s1 = __fadd_rn(x1, __uint_as_float(y & 0xFFFF0000u));
+  }
+  if (SD) {
+    lo = __byte_perm(__float_as_uint(s0), __float_as_uint(s1), 0x5410);
+    hi = __byte_perm(__float_as_uint(s0), __float_as_uint(s1), 0x7632);
+  } else {
+    lo = Elem<bf16_tag>::pack2(s0, s1);
+    hi = 0u;
+  }
+}
+
+// One 16-byte vector (8 elements) of every operand: compute and store.
+template <bool SS, bool SD, bool STREAMING>
+__device__ __forceinline__ void ring_vec_store(uint4 a, uint4 b, uint4 c, uint4* d0, uint4* d1) {
+  uint4 lo, hi;
+  ring_word<SS, SD>(a.x, b.x, c.x, lo.x, hi.x);
+  ring_word<SS, SD>(a.y, b.y, c.y, lo.y, hi.y);
+  ring_word<SS, SD>(a.z, b.z, c.z, lo.z, hi.z);
+  ring_word<SS, SD>(a.w, b.w, c.w, lo.w, hi.w);
+  st_vec<STREAMING>(d0, lo);
+  if (SD) st_vec<STREAMING>(d1, hi);
+}
+
+// 16-byte vectors [0, nv) at byte offset `off` of every buffer (all buffers
+// share one address residue modulo 16); U vectors in flight per thread, all
+// loads issued before the first add.
+template <bool SS, bool SD, int U, bool STREAMING>
+__device__ __forceinline__ void ring_vec_bf16(const char* const* src, char* const* dst, uint64_t off, uint32_t nv) {
+  const uint32_t step = blockDim.x;
+  const uint4* pa = reinterpret_cast<const uint4*>(src[0] + off);
+  const uint4* pb = reinterpret_cast<const uint4*>(src[1] + off);
+  const uint4* pc = reinterpret_cast<const uint4*>(src[SS ? 2 : 1] + off);
+  uint4* d0 = reinterpret_cast<uint4*>(dst[0] + off);
+  uint4* d1 = reinterpret_cast<uint4*>(dst[SD ? 1 : 0] + off);
+  uint32_t v = threadIdx.x;
+  for (; v + (U - 1) * step < nv; v += U * step) {
+    uint4 a[U], b[U], c[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      a[u] = ld_l2(pa + v + u * step);
+      b[u] = ld_l2(pb + v + u * step);
+      c[u] = SS ? ld_l2(pc + v + u * step) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) ring_vec_store<SS, SD, STREAMING>(a[u], b[u], c[u], d0 + v + u * step, d1 + v + u * step);
+  }
+  for (; v < nv; v += step) {
+    const uint4 a = ld_l2(pa + v), b = ld_l2(pb + v);
+    const uint4 c = SS ? ld_l2(pc + v) : make_uint4(0u, 0u, 0u, 0u);
+    ring_vec_store<SS, SD, STREAMING>(a, b, c, d0 + v, d1 + v);
+  }
+}
+
+template <bool SS, bool SD, int U, bool STREAMING>
+__device__ void ring_stage_bf16(const char* const* src, char* const* dst, uint64_t len) {
+  const uint32_t tid = threadIdx.x, nt = blockDim.x;
+  const uint64_t n = len / 2;
+  const uint32_t res = (uint32_t)((uintptr_t)src[0] & 15u);
+  bool co = (((uintptr_t)src[1] & 15u) == res) && (((uintptr_t)dst[0] & 15u) == res);
+  if (SS) co = co && (((uintptr_t)src[2] & 15u) == res);
+  if (SD) co = co && (((uintptr_t)dst[1] & 15u) == res);
+  // buffers at different residues: element by element
+  uint64_t head = co ? ((16u - res) & 15u) / 2 : n;
+  if (head > n) head = n;
+  for (uint64_t k = tid; k < head; k += nt) ring_elem_bf16<SS, SD>(src, dst, k);
+  if (head == n) return;
+  const uint32_t nv = (uint32_t)(((n - head) * 2) >> 4);
+  ring_vec_bf16<SS, SD, U, STREAMING>(src, dst, head * 2, nv);
+  for (uint64_t k = head + (uint64_t)nv * 8 + tid; k < n; k += nt) ring_elem_bf16<SS, SD>(src, dst, k);
+}
+
 // T = void: copy-only kernel (AllGather, AllToAll and their V forms).
 // Otherwise items with one source are the consume-side copies of the
 // two-shot and ring AllReduce, whose source another CTA produced in this
 // launch.  COH: reduce items too may read data produced in this launch (the
-// ring's partial sums), so their loads go through the L2 rather than the
-// non-coherent read-only path.
+// ring's running sums), so their loads go through the L2 rather than the
+// non-coherent read-only path.  `split`: the item's kSplitSrc / kSplitDst bits.
 template <typename T, int NS, int U, bool STREAMING, bool COH>
 __device__ __forceinline__ void run_item(const char* const* src, int ns, char* const* dst, int nd,
-                                         uint64_t len) {
+                                         uint64_t len, uint32_t split) {
   if constexpr (std::is_same<T, void>::value) {
     copy_atom<false, U, STREAMING>(src[0], dst, nd, len);
   } else {
-    if (ns == 1)
+    if (ns == 1) {
       copy_atom<true, 2, STREAMING>(src[0], dst, nd, len);
-    else
+    } else if constexpr (COH && std::is_same<T, bf16_tag>::value) {
+      if (split == (kSplitSrc | kSplitDst))
+        ring_stage_bf16<true, true, U, STREAMING>(src, dst, len);
+      else if (split == kSplitSrc)
+        ring_stage_bf16<true, false, U, STREAMING>(src, dst, len);
+      else if (split == kSplitDst)
+        ring_stage_bf16<false, true, U, STREAMING>(src, dst, len);
+      else
+        reduce_atom<T, NS, U, STREAMING, COH>(src, ns, dst, nd, len);
+    } else {
+      (void)split;
       reduce_atom<T, NS, U, STREAMING, COH>(src, ns, dst, nd, len);
+    }
   }
 }
 
@@ -170,7 +297,7 @@ __global__ void __launch_bounds__(snac_max_threads<NS>(), 2) snac_kernel(const _
   __shared__ char* s_dst[kMaxWorld];
   __shared__ uint64_t s_len;
   __shared__ int s_ns, s_nd, s_ok;
-  __shared__ uint32_t s_item, s_notify, s_epoch, s_wait_ns;
+  __shared__ uint32_t s_item, s_notify, s_epoch, s_wait_ns, s_split;
   __shared__ uint32_t s_next_i, s_q_i;  // thread 0's item cursor (kept out of the registers of the Atoms)
   __shared__ unsigned long long s_t0;
   grid_dep_wait();
@@ -220,9 +347,10 @@ __global__ void __launch_bounds__(snac_max_threads<NS>(), 2) snac_kernel(const _
           const int b = __ffs(m) - 1;
           s_src[ns++] = (b < 16 ? a.in[b] : a.out[b - 16]) + it.src_off;
         }
-        for (uint32_t m = it.dst_mask; m; m &= m - 1) s_dst[nd++] = a.out[__ffs(m) - 1] + it.dst_off;
+        for (uint32_t m = it.dst_mask & kDstRanks; m; m &= m - 1) s_dst[nd++] = a.out[__ffs(m) - 1] + it.dst_off;
         s_ns = ns;
         s_nd = nd;
+        s_split = it.dst_mask & (kSplitSrc | kSplitDst);
         s_len = it.len;
         if (!item_in_bounds(a, it)) {  // checking build: move nothing, keep the SNAC order
           atomicCAS(&a.ctl[kCtlStatus], 0u, (uint32_t)kDevBounds);
@@ -242,9 +370,9 @@ __global__ void __launch_bounds__(snac_max_threads<NS>(), 2) snac_kernel(const _
     const uint32_t i = s_item;
     if (i == kNoItem || !s_ok) break;
     if (a.store_hint == 2)
-      run_item<T, NS, U, true, COH>(s_src, s_ns, s_dst, s_nd, s_len);
+      run_item<T, NS, U, true, COH>(s_src, s_ns, s_dst, s_nd, s_len, s_split);
     else
-      run_item<T, NS, U, false, COH>(s_src, s_ns, s_dst, s_nd, s_len);
+      run_item<T, NS, U, false, COH>(s_src, s_ns, s_dst, s_nd, s_len, s_split);
     __syncthreads();
     if (threadIdx.x == 0) {
       if (s_notify && i + 1 != a.drop_notify) {

@@ -20,8 +20,9 @@ const void* kernel_reduce_bf16(int nsrc, int unroll) {
   }
 }
 
-// Ring AllReduce: two sources per reduce item, one of them a partial sum
-// another CTA stored in this launch (loads through the L2).
+// Ring AllReduce: each reduce stage adds one rank's input to the running
+// binary32 sum another CTA stored, as two 16-bit halves, earlier in this
+// launch (loads through the L2).
 const void* kernel_reduce_ring_bf16(int unroll) {
   return unroll >= 2 ? (const void*)snac_kernel<bf16_tag, 2, 2, true> : (const void*)snac_kernel<bf16_tag, 2, 1, true>;
 }

@@ -9,11 +9,12 @@
 //       rank o owns the o-th of world near-equal element ranges; per tile t of
 //       that range a reduce piece writes out[o] and raises flag (o, t), and a
 //       copy piece waits on the flag and copies out[o] to every other output.
-//   AllReduce, ring  (same page, all_reduce_ring, read as the classic ring):
-//       per tile of chunk j, 2 (world - 1) stages chained by flags: world - 1
-//       reduce pieces of two sources (the next rank's input and the partial
-//       sum the previous stage left in the previous rank's output), then
-//       world - 1 copies that pass the finished tile around the ring.
+//   AllReduce, ring  (same page, all_reduce_ring: a running sum handed from
+//       rank to rank, then the result passed around the ring): per tile,
+//       2 (world - 1) stages chained by flags: world - 1 reduce pieces that
+//       add ranks 1 .. world-1 in ascending order to the binary32 sum the
+//       previous stage left in the outputs, then world - 1 copies that pass
+//       the finished tile around the ring.
 //   ReduceScatter  (NKI, reduce_scatter_hbm_kernel): piece r reduces chunk r of
 //       all inputs into out[r].
 //   AllGather      (NKI, all_gather_hbm_kernel): piece s copies in[s] to offset
@@ -441,22 +442,27 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
               if (t - lag < tiles[o]) copy_piece(o, t - lag);
         }
       } else if (p.tune.layout == kRing && world > 1) {
-        // Ring (Iris docs, "Device Context", all_reduce_ring; the classic
-        // reduce-scatter then all-gather around the ranks).  The range is cut
-        // into `world` chunks and each chunk into tiles.  A tile passes
-        // through 2 (world - 1) stages, each waiting for the previous one's
-        // flag.  Reduce stage k = 1 .. world-1: rank r = j + k (mod world)
-        // folds its input with the partial sum of chunk j -- rank j's input
-        // for k = 1, else the output of rank r - 1 -- into its own output
-        // (rounded to the data type: the partial travels as a buffer of it).
-        // After stage world-1 rank j - 1 holds the finished chunk.  Gather
-        // stage m = 1 .. world-1: the output of rank j - 2 + m is copied to
-        // rank j - 1 + m.  Every output byte but those of ranks j - 1 and j is
-        // written twice, partial first, and the overwrite waits (through the
-        // chain) for the read of the partial.
+        // Ring (Iris docs, "Device Context", all_reduce_ring: a running sum
+        // handed from rank to rank, then the finished data passed around the
+        // ring).  The range is cut into `world` chunks and each chunk into
+        // tiles (the chunks only order the tiles).  A tile passes through
+        // 2 (world - 1) stages, each waiting for the previous one's flag.
+        // Reduce stage k = 1 .. world-1 adds rank k's input to the running
+        // sum (stage 1: rank 0's input plus rank 1's), so every tile is
+        // folded in ascending rank order from rank 0, in binary32, with one
+        // rounding at the end: the ascending fold, bit for bit.  The sum
+        // lives in the outputs between stages: fp32 in rank k's output; bf16
+        // as two 16-bit halves (kSplitDst), low half in rank k - 1's output,
+        // high half in rank k's.  The last reduce stage stores the rounded
+        // value to rank world-1's output.  Gather stage m = 1 .. world-1
+        // copies the output of rank world-2+m (mod world) to rank
+        // world-1+m (mod world).  Every output byte is written more than once
+        // (the sum first, the result last) and each overwrite waits, through
+        // the chain, for the read of what it replaces.
         if (p.tune.path != kPathRegister) return PL_ERR_UNSUPPORTED;  // the register-path kernel only
         sync = true;
         p.nsrc = 2;
+        const bool split = dtype == kBF16;
         const uint64_t n = S / E;
         const uint64_t T = std::max<uint64_t>(16, (uint64_t)p.tune.chunk_bytes / 16 * 16);
         uint64_t start[kMaxWorld + 1];
@@ -484,16 +490,28 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
           const uint64_t off = start[j] + t * T, len = std::min(T, start[j + 1] - off);
           uint32_t src, dst;
           if (st + 1 < (uint32_t)world) {
-            const int k = (int)st + 1, r = (j + k) % world, prev = (j + k - 1) % world;
-            src = (1u << r) | (k == 1 ? (1u << prev) : (1u << (16 + prev)));
-            dst = 1u << r;
+            const int k = (int)st + 1;
+            const bool last = k == world - 1;
+            if (k == 1)
+              src = 1u | 2u;                                  // rank 0's input + rank 1's
+            else if (split)
+              src = (1u << k) | (3u << (16 + k - 2));         // rank k's input + halves in outputs k-2, k-1
+            else
+              src = (1u << k) | (1u << (16 + k - 1));         // rank k's input + the sum in output k-1
+            dst = (last || !split) ? (1u << k) : (3u << (k - 1));
+            if (split && k > 1) dst |= kSplitSrc;
+            if (split && !last) dst |= kSplitDst;
           } else {
             const int m = (int)st - (world - 1) + 1;
-            src = 1u << (16 + (j - 2 + m + 2 * world) % world);
-            dst = 1u << ((j - 1 + m + world) % world);
+            src = 1u << (16 + (world - 2 + m) % world);
+            dst = 1u << ((world - 1 + m) % world);
           }
           Piece q{off, off, len, src, dst, st ? flag(j, t, st - 1) : 0u, st + 1 < stages ? flag(j, t, st) : 0u};
-          push_grouped(pieces, q, dst_res);
+          if (dst & (kSplitSrc | kSplitDst)) {
+            if (q.len) pieces.push_back(q);  // one item: the halves are two values, not copies of one
+          } else {
+            push_grouped(pieces, q, dst_res);
+          }
         };
         for (uint64_t step = 0; step < tmax + (uint64_t)(stages - 1) * lag; ++step)
           for (uint32_t st = 0; st < stages; ++st) {
@@ -769,10 +787,23 @@ std::string check_plan(const Plan& p) {
     const Item& it = p.items[i];
     if (it.len == 0) return "empty item";
     const uint32_t in_bits = it.src_mask & 0xFFFFu, out_bits = it.src_mask >> 16;
+    const uint32_t dst_bits = it.dst_mask & kDstRanks, split = it.dst_mask & (kSplitSrc | kSplitDst);
     if ((in_bits & ~ALL) || (out_bits & ~ALL)) return "source mask outside the world";
-    if (!it.dst_mask || (it.dst_mask & ~ALL)) return "destination mask empty or outside the world";
+    if (!dst_bits || (dst_bits & ~ALL) || (it.dst_mask & ~(kDstRanks | kSplitSrc | kSplitDst)))
+      return "destination mask empty or outside the world";
     const int nsrc = popcount32(it.src_mask);
     if (nsrc < 1) return "item without a source";
+    if (split) {
+      // the ring's binary32 running sum over bf16 data: two output halves in
+      // neighbouring ranks, read and / or written by one reduce item
+      if (p.tune.layout != kRing || p.dtype != kBF16 || nsrc < 2) return "split sum outside the bf16 ring";
+      if ((it.dst_mask & kSplitSrc) && (popcount32(out_bits) != 2 || (out_bits & (out_bits >> 1)) == 0))
+        return "split source is not two neighbouring outputs";
+      if ((it.dst_mask & kSplitDst) && (popcount32(dst_bits) != 2 || (dst_bits & (dst_bits >> 1)) == 0))
+        return "split destination is not two neighbouring outputs";
+    } else if (nsrc > 1 && popcount32(out_bits) > 1) {
+      return "a reduce reads several outputs";
+    }
     // a reduce reads an output only in the ring layout (whose kernel loads
     // such sources through the L2) and only after waiting for its producer
     if (nsrc > 1 && out_bits && (p.tune.layout != kRing || !it.wait)) return "a reduce reads outputs";
@@ -789,7 +820,7 @@ std::string check_plan(const Plan& p) {
       if (it.src_off + it.len > p.out_bytes[r]) return "reads past an output";
       acc[r].push_back({it.src_off, it.src_off + it.len, (int64_t)i, false});
     }
-    for (uint32_t m = it.dst_mask; m; m &= m - 1) {
+    for (uint32_t m = dst_bits; m; m &= m - 1) {
       int r = __builtin_ctz(m);
       if (it.dst_off + it.len > p.out_bytes[r]) {
         err << "item " << i << " writes past output " << r;

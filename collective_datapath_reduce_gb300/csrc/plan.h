@@ -55,11 +55,21 @@ struct Item {
   uint64_t dst_off;
   uint64_t len;
   uint32_t src_mask;  // bit r: input of rank r; bit 16 + r: output of rank r
-  uint32_t dst_mask;  // bit r: output of rank r
+  uint32_t dst_mask;  // bit r: output of rank r; bits 30, 31: kSplitSrc, kSplitDst
   uint32_t wait;      // 0 or flag index + 1
   uint32_t notify;    // 0 or flag index + 1
 };
 static_assert(sizeof(Item) == 40, "device item layout");
+
+// Ring AllReduce over bf16 data: the running sum is a binary32 value kept as
+// two 16-bit halves in two rank outputs, the low half in the lower-numbered
+// rank, the high half in the higher-numbered one.  kSplitSrc: the item's two
+// output sources are those halves (its input sources are added to the sum
+// they form).  kSplitDst: its two destinations receive the halves of the new
+// sum instead of a rounded bf16 value.  Only the ring kernel reads them.
+constexpr uint32_t kSplitSrc = 1u << 30;
+constexpr uint32_t kSplitDst = 1u << 31;
+constexpr uint32_t kDstRanks = 0xFFFFu;
 
 struct Tune {
   int layout = 0;

@@ -12,8 +12,6 @@ from .collectives import (  # noqa: F401
     f32_to_bf16_rne,
     fold_sum,
     all_reduce,
-    all_reduce_ring,
-    ring_chunk_bounds,
     reduce_scatter,
     reduce_scatter_v,
     all_gather,

@@ -6,10 +6,6 @@ Sources, by page and section:
          across ranks, all-gather gathers along dim 0, reduce-scatter sums then
          scatters dim-0 chunks, all-to-all exchanges dim-0 chunks); the
          all_to_all_hbm_kernel entry (rank i receives chunk i of every input).
-  [IRIS] Iris docs, "Device Context", collective operations: all_reduce_ring
-         (a tile-level all-reduce by the ring algorithm; the page names the
-         algorithm only, so the classic reduce-scatter-then-all-gather ring
-         is written out below).
   [PUR]  Purlin README (purlin 0.6.4 PKG-INFO), summary paragraph: the
          collectives are AllReduce, AllGather, ReduceScatter, AllToAll and
          variable-length variants of the last three; the datapath primitives are
@@ -24,10 +20,6 @@ design notes of the repository):
   * ReduceScatter / AllToAll split dim 0 into `world` equal chunks; a size that
     does not split evenly is an error.
   * AllToAll places the chunk received from rank s at output chunk s.
-  * The ring AllReduce (an explicitly chosen layout, not the default) follows
-    the classic ring: chunk j's partial sum starts at rank j and gains one
-    rank per hop around the ring; the partial travels in the data type, so a
-    bf16 partial is rounded at every hop.
   * The V variants take per-rank (AllGatherV, ReduceScatterV) or per
     (source, destination) pair (AllToAllV) element counts; data are packed
     with prefix-sum displacements in rank order.
@@ -166,45 +158,6 @@ def reduce_scatter_v(inputs: list[np.ndarray], counts: list[int], dtype: str) ->
         out.append(_narrow(fold_sum(cols), dtype))
         start += c
     return out
-
-
-def ring_chunk_bounds(n: int, world: int) -> list[int]:
-    """Element bounds of the ring's `world` chunks: chunk j holds n // world
-    elements, plus one for the first n % world chunks, in order."""
-    bounds = [0]
-    for j in range(world):
-        bounds.append(bounds[-1] + n // world + (1 if j < n % world else 0))
-    return bounds
-
-
-def all_reduce_ring(inputs: list[np.ndarray], dtype: str) -> list[np.ndarray]:
-    """AllReduce by the ring algorithm [IRIS] all_reduce_ring.
-
-    The buffer is cut into `world` chunks (ring_chunk_bounds).  Chunk j's sum
-    travels the ring starting at rank j: the partial sum begins as rank j's
-    elements; at each hop k = 1 .. world-1 rank (j + k) mod world adds its own
-    elements to the partial it received, in binary32, and rounds the result to
-    the data type, because the partial is passed on as a buffer of that type.
-    The last partial (held by rank j - 1) is then passed around the ring
-    unchanged, so every rank receives the same sums.  Compared with
-    all_reduce(), the order of the adds differs per chunk and bf16 sums are
-    rounded at every hop; for fp32 and two ranks the results are the same.
-    """
-    world = _check_ranks(inputs)
-    n = inputs[0].size
-    if any(b.size != n for b in inputs):
-        raise ValueError("all-reduce buffers must have equal length")
-    bounds = ring_chunk_bounds(n, world)
-    result = np.empty_like(inputs[0])
-    for j in range(world):
-        lo, hi = bounds[j], bounds[j + 1]
-        partial = np.array(inputs[j][lo:hi], copy=True)
-        for k in range(1, world):
-            r = (j + k) % world
-            acc = np.add(_widen(partial, dtype), _widen(inputs[r][lo:hi], dtype), dtype=np.float32)
-            partial = _narrow(acc, dtype)
-        result[lo:hi] = partial
-    return [result.copy() for _ in range(world)]
 
 
 # --------------------------------------------------------------------------

@@ -126,37 +126,3 @@ def all_to_all_v(ins, C):
             off = sum(C[s][k] for k in range(d))
             out[d].extend(ins[s][off:off + C[s][d]])
     return out
-
-
-def all_reduce_ring(ins, dtype):
-    """Ring all-reduce simulated as messages between ranks, step by step.
-
-    Reduce-scatter: in step t (0 .. N-2) every rank r sends its chunk
-    (r - t) mod N to rank r + 1, which adds the message to its own values of
-    that chunk and keeps the sum in the data type.  All messages of a step are
-    taken before any is applied.  Afterwards rank r holds the finished chunk
-    (r + 1) mod N.  All-gather: in step t rank r sends chunk (r + 1 - t) mod N
-    to rank r + 1, which overwrites its copy.  Chunk j holds n // N elements,
-    one more for j < n % N.
-    """
-    N, n = len(ins), len(ins[0])
-    sizes = [n // N + (1 if j < n % N else 0) for j in range(N)]
-    starts = [sum(sizes[:j]) for j in range(N)]
-    idx = [range(starts[j], starts[j] + sizes[j]) for j in range(N)]
-    buf = [list(b) for b in ins]
-
-    def add(own, msg):
-        s = f32(_widen(own, dtype) + _widen(msg, dtype))
-        return s if dtype == "f32" else bf16_round(s)
-
-    for t in range(N - 1):
-        msgs = [((r + 1) % N, (r - t) % N, [buf[r][i] for i in idx[(r - t) % N]]) for r in range(N)]
-        for d, j, vals in msgs:
-            for i, v in zip(idx[j], vals):
-                buf[d][i] = add(buf[d][i], v)
-    for t in range(N - 1):
-        msgs = [((r + 1) % N, (r + 1 - t) % N, [buf[r][i] for i in idx[(r + 1 - t) % N]]) for r in range(N)]
-        for d, j, vals in msgs:
-            for i, v in zip(idx[j], vals):
-                buf[d][i] = v
-    return buf

@@ -3,13 +3,19 @@
 This checks the layout engine and the tiling without a GPU: the items are
 applied in their global order (every wait refers to an earlier notify), a
 reduce item folds its sources in ascending mask-bit order in binary32 and
-rounds to the output type, a copy item moves bytes.  The result must equal
-the oracle's.  It is a test of which bytes go where, not a second datapath.
+rounds to the output type, a copy item moves bytes.  The ring layout's bf16
+items may carry a binary32 running sum as two 16-bit halves in two outputs
+(destination-mask bit 30: two of the sources are those halves, low half in
+the lower rank; bit 31: the two destinations receive the new sum's halves).
+The result must equal the oracle's.  It is a test of which bytes go where,
+not a second datapath.
 """
 
 import numpy as np
 
 import oracle
+
+SPLIT_SRC, SPLIT_DST = 1 << 30, 1 << 31
 
 
 def run_items(items, ins, outs, dtype):
@@ -27,14 +33,26 @@ def run_items(items, ins, outs, dtype):
             m >>= 1
             b += 1
         dsts = [r for r in range(16) if (it["dst_mask"] >> r) & 1]
+        split_src, split_dst = bool(it["dst_mask"] & SPLIT_SRC), bool(it["dst_mask"] & SPLIT_DST)
         if len(srcs) == 1:
             val = srcs[0].copy()
         else:
             if dtype == "f32":
                 cols = [s.view(np.float32) for s in srcs]
-                val = oracle.fold_sum(cols).view(np.uint8)
+                acc = oracle.fold_sum(cols)
             else:
-                cols = [oracle.bf16_bits_to_f32(s.view(np.uint16)) for s in srcs]
-                val = oracle.f32_to_bf16_rne(oracle.fold_sum(cols)).view(np.uint8)
+                if split_src:          # input sources, then the low and high halves
+                    lo, hi = (s.view(np.uint16).astype(np.uint32) for s in srcs[-2:])
+                    cols = [((hi << np.uint32(16)) | lo).view(np.float32)]
+                    cols += [oracle.bf16_bits_to_f32(s.view(np.uint16)) for s in srcs[:-2]]
+                else:
+                    cols = [oracle.bf16_bits_to_f32(s.view(np.uint16)) for s in srcs]
+                acc = oracle.fold_sum(cols)
+            if split_dst:
+                b = acc.view(np.uint32)
+                outs[dsts[0]][do:do + n] = (b & np.uint32(0xFFFF)).astype(np.uint16).view(np.uint8)
+                outs[dsts[1]][do:do + n] = (b >> np.uint32(16)).astype(np.uint16).view(np.uint8)
+                continue
+            val = acc.view(np.uint8) if dtype == "f32" else oracle.f32_to_bf16_rne(acc).view(np.uint8)
         for d in dsts:
             outs[d][do:do + n] = val

@@ -282,61 +282,6 @@ def pin_brute_force(oracle, seed=7):
                 assert list(got[r]) == w
 
 
-# ------------------------------------------------------------ ring order
-
-def pin_ring(oracle, seed=13):
-    """The ring all-reduce (an explicitly chosen layout).
-
-    Hand-worked cases, three ranks, one element per chunk (chunk j = element j):
-      fp32, ranks [1e8, 1, -1e8]: chunk j is folded from rank j around the ring,
-        j=0: (1e8 + 1) - 1e8 = 0;  j=1: (1 - 1e8) + 1e8 = 0 (1 - 1e8 rounds to
-        -1e8: the ulp at 1e8 is 8);  j=2: (-1e8 + 1e8) + 1 = 1.
-      bf16, ranks [1, 2^-8, 2^-8] (0x3F80, 0x3B80): 1 + 2^-8 is a tie between
-        1 and 1 + 2^-7 and rounds to the even pattern 1.0 at every hop,
-        j=0: 1.0;  j=1: 2^-8 + 2^-8 = 2^-7 exact, + 1 = 0x3F81;  j=2: 1.0.
-        One rounding at the end would give 0x3F81 everywhere.
-      fp32, n = 7: chunks of 3, 2, 2 elements -> [0, 0, 0, 0, 0, 1, 1].
-    Two ranks: a + b = b + a exactly, so the ring equals the ascending fold.
-    Integer data: exact whatever the order.  One rank: a copy.  And the
-    message-passing simulation of brute.py on tiny inputs.
-    """
-    x = [np.array([v] * 3, dtype=np.float32) for v in (1e8, 1.0, -1e8)]
-    got = oracle.all_reduce_ring(x, "f32")
-    for r in range(3):
-        assert list(got[r]) == [0.0, 0.0, 1.0], got[r]
-    b = [np.array([h] * 3, dtype=np.uint16) for h in (0x3F80, 0x3B80, 0x3B80)]
-    got = oracle.all_reduce_ring(b, "bf16")
-    for r in range(3):
-        assert [int(v) for v in got[r]] == [0x3F80, 0x3F81, 0x3F80], [hex(int(v)) for v in got[r]]
-    x7 = [np.array([v] * 7, dtype=np.float32) for v in (1e8, 1.0, -1e8)]
-    assert list(oracle.all_reduce_ring(x7, "f32")[1]) == [0, 0, 0, 0, 0, 1, 1]
-    rng = np.random.default_rng(seed)
-    y = rng.standard_normal((2, 301)).astype(np.float32)
-    for dtype in ("f32", "bf16"):
-        ins = [y[s] if dtype == "f32" else oracle.f32_to_bf16_rne(y[s]) for s in range(2)]
-        ring, asc = oracle.all_reduce_ring(ins, dtype), oracle.all_reduce(ins, dtype)
-        assert eq_bits(ring[0], asc[0]) and eq_bits(ring[1], asc[1])
-    from collective_datapath_reduce_gb300 import inputs
-    xi = inputs.w1_allreduce_ints(5, 103, 3)
-    exact = xi.astype(np.int64).sum(axis=0)
-    for dtype in ("f32", "bf16"):
-        outs = oracle.all_reduce_ring([to_dtype(xi[s], dtype) for s in range(5)], dtype)
-        for r in range(5):
-            assert np.array_equal(from_dtype(outs[r], dtype).astype(np.int64), exact), (dtype, r)
-    one = [np.arange(5, dtype=np.float32)]
-    assert eq_bits(oracle.all_reduce_ring(one, "f32")[0], one[0])
-    for world in range(1, 6):
-        for n in range(0, 13):
-            z = (rng.standard_normal((world, n)) * 3).astype(np.float32)
-            for dtype in ("f32", "bf16"):
-                ins = [z[s] if dtype == "f32" else oracle.f32_to_bf16_rne(z[s]) for s in range(world)]
-                py = [[float(v) for v in q] if dtype == "f32" else [int(v) for v in q] for q in ins]
-                got = oracle.all_reduce_ring(ins, dtype)
-                want = brute.all_reduce_ring(py, dtype)
-                for r in range(world):
-                    assert eq_bits(got[r], np.asarray(want[r], dtype=got[r].dtype)), ("ring", world, n, dtype, r)
-
-
 ALL_PINS = [
     pin_worked_example,
     pin_dim0_definitions,
@@ -347,5 +292,4 @@ ALL_PINS = [
     pin_error_bound,
     pin_invariants,
     pin_brute_force,
-    pin_ring,
 ]

@@ -119,8 +119,7 @@ def test_limited_output_is_caught(checking, tune):
         P.check(P.purlin_all_reduce(h.h, src.ptrs(), dst.ptrs(), n * 2, P.PL_BF16, 0, stream()))
         sync()
         assert h.status() == 0
-        ring = tune.get("layout") == P.PL_LAYOUT_RING
-        want = oracle.all_reduce_ring(ins, "bf16") if ring else oracle.all_reduce(ins, "bf16")
+        want = oracle.all_reduce(ins, "bf16")
         for r in range(world):
             assert np.array_equal(dst.read(r, np.uint16), want[r])
     finally:

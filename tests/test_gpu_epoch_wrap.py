@@ -36,7 +36,7 @@ TUNES = [
     ("two_shot", {"layout": P.PL_LAYOUT_TWO_SHOT, "chunk_bytes": 16384}, oracle.all_reduce),
     ("two_shot_bulk", {"layout": P.PL_LAYOUT_TWO_SHOT, "chunk_bytes": 4096, "path": P.PATH_BULK, "stages": 2},
      oracle.all_reduce),
-    ("ring", {"layout": P.PL_LAYOUT_RING, "chunk_bytes": 16384}, oracle.all_reduce_ring),
+    ("ring", {"layout": P.PL_LAYOUT_RING, "chunk_bytes": 16384}, oracle.all_reduce),
 ]
 
 
@@ -52,6 +52,8 @@ def test_results_and_flags_across_the_epoch_wrap(name, tune, ref):
     dst = RankBuffers([n * 2] * world)
     try:
         P.check(P.purlin_tune_override(h.h, tune))
+        # the counter never holds 0xFFFFFFFF (the next launch would take epoch 0)
+        assert P.purlin_debug_set_epoch(h.h, 0xFFFFFFFF, stream()) == P.PL_ERR_INVALID_ARG
         P.check(P.purlin_debug_set_epoch(h.h, 0xFFFFFFFD, stream()))
         for k, expect in enumerate([0xFFFFFFFE, 0, 1, 2]):
             ins = [inputs.to_bf16_bits(RNG.standard_normal(n).astype(np.float32)) for _ in range(world)]

@@ -184,7 +184,7 @@ def test_two_shot_on_pinned_host_buffers():
 
 
 def test_ring_on_pinned_host_buffers():
-    """The ring's partial sums live in host memory between hops (loads through the L2)."""
+    """The ring's running sums live in host memory between stages (loads through the L2)."""
     world, n = 4, (1 << 17) + 3
     ins = [inputs.to_bf16_bits(RNG.standard_normal(n).astype(np.float32)) for _ in range(world)]
     src = [pinned(x) for x in ins]
@@ -192,7 +192,7 @@ def test_ring_on_pinned_host_buffers():
     h = Handle(world)
     try:
         P.check(P.purlin_tune_override(h.h, {"layout": P.PL_LAYOUT_RING, "chunk_bytes": 16384}))
-        want = oracle.all_reduce_ring(ins, "bf16")
+        want = oracle.all_reduce(ins, "bf16")
         for _ in range(2):
             P.check(P.purlin_all_reduce(h.h, src, dst, n * 2, P.PL_BF16, 0, stream()))
             sync()

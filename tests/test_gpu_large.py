@@ -95,7 +95,6 @@ def ar_inputs():
     torch.cuda.empty_cache()
 
 
-# (two ranks: the ring's sums equal the ascending fold, a + b = b + a)
 @pytest.mark.parametrize("layout", [P.PL_LAYOUT_AUTO, P.PL_LAYOUT_TWO_SHOT, P.PL_LAYOUT_RING])
 def test_all_reduce_2x2_5GiB(ar_inputs, layout):
     S, n, T, src = ar_inputs

@@ -3,7 +3,7 @@
 Covers every collective, worlds 1..16, sizes with ragged tails, unaligned
 V counts, buffer addresses with mixed residues modulo 16, tiny grids (many
 items per CTA) and big grids (many CTAs per piece), and the three AllReduce
-layouts (the ring against the ring oracle).  Also checks the plan's
+layouts (all three against the one ascending fold).  Also checks the plan's
 bookkeeping: CTA assignment and the SNAC rule that every wait follows its
 notify in global order.
 """
@@ -89,13 +89,25 @@ def test_all_reduce_plan(world, dtype, layout):
                         assert it["cta"] == i % grid
 
 
+SPLIT_SRC, SPLIT_DST = 1 << 30, 1 << 31
+
+
+def _ring_chunk_tiles(n, world, E, tile):
+    """Tiles of the ring plan: `world` chunks of n // world elements (one more
+    for the first n % world), each cut into tiles of `tile` bytes."""
+    sizes = [(n // world + (1 if j < n % world else 0)) * E for j in range(world)]
+    return sum(-(-b // tile) for b in sizes)
+
+
 @pytest.mark.parametrize("world", [1, 2, 3, 8, 16])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_ring_all_reduce_plan(world, dtype):
-    """The ring layout, run item by item on the host, gives the ring oracle's
-    result; its chains are ordered (every wait after its notify, each tile's
-    stages one after another), the overwrite of every partial sum waits for
-    the read of it, and the CTAs run their items in increasing global order."""
+    """The ring layout, run item by item on the host, gives the ascending fold
+    (the oracle's AllReduce) bit for bit; its chains are ordered (every wait
+    after its notify, each tile's stages one after another), every reduce
+    stage adds the next rank in ascending order, the overwrite of every
+    running sum waits for the read of it, and the CTAs run their items in
+    increasing global order."""
     E = ESZ[dtype]
     for n in (1, 7, 1000, 4096 + 3):
         for sm in SMS:
@@ -106,26 +118,40 @@ def test_ring_all_reduce_plan(world, dtype):
             items, grid, nflags = _describe(P.PL_COLL_ALL_REDUCE, world, DT[dtype], [n * E], sres, dres, sm, tune)
             outs = [np.zeros(n * E, np.uint8) for _ in range(world)]
             run_items(items, [_bytes(x) for x in ins], outs, dtype)
-            want = oracle.all_reduce_ring(ins, dtype)
+            want = oracle.all_reduce(ins, dtype)
             for r in range(world):
                 assert np.array_equal(outs[r], _bytes(want[r])), (n, sm, r)
             if world == 1:
                 continue
             assert nflags > 0
-            notify_at = {}
+            notify_at, stage_of = {}, {}
             for i, it in enumerate(items):
-                assert popcount(it["src_mask"]) in (1, 2) and popcount(it["dst_mask"]) == 1
+                ins_bits, out_bits = it["src_mask"] & 0xFFFF, it["src_mask"] >> 16
+                dst_bits = it["dst_mask"] & 0xFFFF
+                split_src, split_dst = bool(it["dst_mask"] & SPLIT_SRC), bool(it["dst_mask"] & SPLIT_DST)
                 if it["wait"]:
                     assert it["wait"] in notify_at and notify_at[it["wait"]] < i
+                    k = stage_of[it["wait"]] + 1
                 else:
-                    # a tile's first stage: reduce of two inputs
-                    assert it["src_mask"] >> 16 == 0 and popcount(it["src_mask"]) == 2
+                    k = 1          # a tile's first stage: rank 0's input plus rank 1's
+                    assert ins_bits == 3 and out_bits == 0
+                if k < world:      # reduce stage k adds rank k's input to the running sum
+                    assert k == 1 or ins_bits == 1 << k
+                    if k > 1:
+                        assert out_bits == ((3 << (k - 2)) if dtype == "bf16" else (1 << (k - 1)))
+                    assert split_src == (dtype == "bf16" and k > 1)
+                    assert split_dst == (dtype == "bf16" and k < world - 1)
+                    assert dst_bits == ((3 << (k - 1)) if split_dst else (1 << k))
+                else:              # gather stage: the finished tile passed on around the ring
+                    m = k - (world - 1)
+                    assert ins_bits == 0 and out_bits == 1 << ((world - 2 + m) % world)
+                    assert dst_bits == 1 << ((world - 1 + m) % world) and not (split_src or split_dst)
                 assert it["cta"] == i % grid
                 if it["notify"]:
                     notify_at[it["notify"]] = i
+                    stage_of[it["notify"]] = k
             stages = 2 * world - 2
-            tiles = sum(-(-b // 1024) for b in np.diff([x * E for x in oracle.ring_chunk_bounds(n, world)]))
-            assert len(items) == tiles * stages
+            assert len(items) == _ring_chunk_tiles(n, world, E, 1024) * stages
 
 
 def test_ring_tiles_follow_the_chunk_size():
@@ -412,3 +438,27 @@ def test_guided_queue_plans():
     st, items, _, _ = P.purlin_plan_describe(P.PL_COLL_ALL_REDUCE, world, P.PL_F32, [1 << 22], None, None, 152,
                                              {"schedule": P.PL_SCHED_QUEUE_GUIDED, "interleave_bytes": 4096})
     assert st == P.PL_OK and items[0]["len"] > items[-1]["len"]
+
+
+def _header_define(name):
+    import os
+    import re
+    from collective_datapath_reduce_gb300 import _build
+    with open(os.path.join(_build.INCLUDE, "purlin_gb.h")) as f:
+        return int(re.search(rf"#define {name} (\d+)u?", f.read()).group(1))
+
+
+def test_default_workspace_holds_the_snac_layouts_flags():
+    """The workspace a handle gets without a caller's one holds the two-shot
+    and ring layouts' flags at the table's tile sizes up to the sizes the
+    header states (8 ranks of 9 GiB, 16 of 4 GiB), so such calls never grow
+    it; purlin_workspace_bytes sizes a workspace for a larger maximum."""
+    default = _header_define("PURLIN_DEFAULT_WORKSPACE_FLAGS")
+    GiB = 1 << 30
+    for world, S in ((8, 9 * GiB), (16, 4 * GiB), (2, 64 * GiB), (8, 64 << 20)):
+        for layout in (P.PL_LAYOUT_TWO_SHOT, P.PL_LAYOUT_RING):
+            st, _, _, nflags = P.purlin_plan_describe(P.PL_COLL_ALL_REDUCE, world, P.PL_BF16, [S], None, None, 152,
+                                                      {"layout": layout}, items=False)
+            assert st == P.PL_OK
+            assert nflags <= default, (world, S, layout, nflags)
+            assert P.purlin_workspace_bytes(world, S) >= 256 + 4 * nflags

@@ -14,7 +14,7 @@ import oracle.collectives as oc
 import pins
 
 PUBLIC = [
-    "bf16_bits_to_f32", "f32_to_bf16_rne", "fold_sum", "all_reduce", "all_reduce_ring", "reduce_scatter",
+    "bf16_bits_to_f32", "f32_to_bf16_rne", "fold_sum", "all_reduce", "reduce_scatter",
     "reduce_scatter_v", "all_gather", "all_to_all", "all_gather_v", "all_to_all_v",
 ]
 
@@ -116,38 +116,7 @@ def _a2av_send_displ_wrong(inputs, counts):
     return out
 
 
-def _ring_mutant(start_shift=0, per_hop=True, split="even"):
-    """A ring all-reduce with one planted mistake."""
-    def ring(inputs, dtype):
-        world, n = len(inputs), inputs[0].size
-        if split == "even":
-            bounds = oc.ring_chunk_bounds(n, world)
-        else:                                   # the last chunk takes the remainder
-            q = n // world
-            bounds = [j * q for j in range(world)] + [n]
-        result = np.empty_like(inputs[0])
-        for j in range(world):
-            lo, hi = bounds[j], bounds[j + 1]
-            order = [(j + start_shift + k) % world for k in range(world)]
-            acc = oc._widen(inputs[order[0]][lo:hi], dtype).astype(np.float32)
-            for r in order[1:]:
-                acc = np.add(acc, oc._widen(inputs[r][lo:hi], dtype), dtype=np.float32)
-                if per_hop:
-                    acc = oc._widen(oc._narrow(acc, dtype), dtype)
-            result[lo:hi] = oc._narrow(acc, dtype)
-        return [result.copy() for _ in range(world)]
-    return ring
-
-
-def _ring_ascending(inputs, dtype):
-    return oc.__dict__["_orig_ar"](inputs, dtype)
-
-
 MUTANTS = {
-    "ring_starts_one_rank_late": {"all_reduce_ring": _ring_mutant(start_shift=1)},
-    "ring_rounds_once": {"all_reduce_ring": _ring_mutant(per_hop=False)},
-    "ring_remainder_in_last_chunk": {"all_reduce_ring": _ring_mutant(split="last")},
-    "ring_is_ascending_fold": {"all_reduce_ring": _ring_ascending},
     "fold_descending": {"fold_sum": _fold_descending},
     "fold_drops_last_rank": {"fold_sum": _fold_drop_last},
     "fold_from_positive_zero": {"fold_sum": _fold_from_zero},
@@ -169,7 +138,6 @@ MUTANTS = {
 def test_mutant_is_caught(name, monkeypatch):
     monkeypatch.setitem(oc.__dict__, "_orig_fold", oc.fold_sum)
     monkeypatch.setitem(oc.__dict__, "_orig_rs", oc.reduce_scatter)
-    monkeypatch.setitem(oc.__dict__, "_orig_ar", oc.all_reduce)
     monkeypatch.setitem(oc.__dict__, "_orig_ag", oc.all_gather)
     monkeypatch.setitem(oc.__dict__, "_orig_agv", oc.all_gather_v)
     ns = types.SimpleNamespace(**{k: getattr(oc, k) for k in PUBLIC})

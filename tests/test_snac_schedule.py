@@ -53,7 +53,7 @@ def run_threads(items, grid, ins, outs, dtype, drop=None, timeout=5.0):
     return not status["failed"]
 
 
-LAYOUTS = [(P.PL_LAYOUT_TWO_SHOT, oracle.all_reduce), (P.PL_LAYOUT_RING, oracle.all_reduce_ring)]
+LAYOUTS = [(P.PL_LAYOUT_TWO_SHOT, oracle.all_reduce), (P.PL_LAYOUT_RING, oracle.all_reduce)]
 
 
 @pytest.mark.parametrize("sm", [1, 3, 16])
@@ -61,7 +61,7 @@ LAYOUTS = [(P.PL_LAYOUT_TWO_SHOT, oracle.all_reduce), (P.PL_LAYOUT_RING, oracle.
 @pytest.mark.parametrize("layout,ref", LAYOUTS, ids=["two_shot", "ring"])
 def test_snac_schedule_completes_under_threads(sm, world, layout, ref):
     """Two-shot: one wait per copy.  Ring: a chain of 2 (world - 1) stages per
-    tile, whose partial sums are overwritten later in the same chain."""
+    tile, whose running sums are overwritten later in the same chain."""
     rng = np.random.default_rng(world * 100 + sm)
     n = 5000 * world + 3
     ins = [oracle.f32_to_bf16_rne(rng.standard_normal(n).astype(np.float32)) for _ in range(world)]
