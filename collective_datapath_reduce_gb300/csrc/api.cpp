@@ -24,7 +24,9 @@
 namespace {
 
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
-constexpr size_t kDefaultFlags = 64 * 1024;  // library-owned workspace starts with 256 KiB of flags
+// Library-owned workspace: flags for the two-shot and ring AllReduce layouts
+// at the table's tile sizes up to several GiB per rank (4 MiB of flags).
+constexpr size_t kDefaultFlags = PURLIN_DEFAULT_WORKSPACE_FLAGS;
 
 struct DevPlan {
   pl::Plan plan;
@@ -51,6 +53,7 @@ struct purlin_ctx {
   void* ws = nullptr;
   size_t ws_bytes = 0;
   bool ws_owned = false;
+  int ws_grown = 0;             // times the library-owned workspace was enlarged
   uint32_t* ctl = nullptr;
   uint32_t* flags = nullptr;
   size_t flag_cap = 0;
@@ -165,6 +168,7 @@ purlin_status ensure_flags(purlin_ctx* h, size_t need, cudaStream_t stream) {
   cudaFree(h->ws);
   h->ws = nws;
   h->ws_bytes = bytes;
+  h->ws_grown += 1;
   h->ctl = (uint32_t*)nws;
   h->flags = (uint32_t*)((char*)nws + pl::kCtlBytes);
   h->flag_cap = cap;
@@ -498,7 +502,8 @@ purlin_status purlin_initialize(int world, void* workspace, size_t workspace_byt
     h->ws_bytes = workspace_bytes;
     h->ws_owned = false;
   } else {
-    h->ws_bytes = pl::kCtlBytes + kDefaultFlags * sizeof(uint32_t);
+    // NULL workspace: the library allocates the default, or workspace_bytes if larger
+    h->ws_bytes = std::max(workspace_bytes, pl::kCtlBytes + kDefaultFlags * sizeof(uint32_t));
     if ((e = cudaMalloc(&h->ws, h->ws_bytes)) != cudaSuccess) return cuda_fail(e);
     h->ws_owned = true;
   }
@@ -784,6 +789,9 @@ purlin_status purlin_debug_drop_notify(purlin_handle h, long long item) {
 purlin_status purlin_debug_set_epoch(purlin_handle h, uint32_t epoch, purlin_stream_t stream) {
   purlin_status st;
   if ((st = check_handle(h))) return st;
+  // the counter holds the epoch the last launch used, 0 .. 0xFFFFFFFE: from
+  // 0xFFFFFFFF the next launch would take epoch 0, the value of cleared flags
+  if (epoch == 0xFFFFFFFFu) return PL_ERR_INVALID_ARG;
   if (capturing((cudaStream_t)stream)) return PL_ERR_INVALID_ARG;  // a captured copy would read a dead stack slot
   std::lock_guard<std::mutex> lock(h->mu);
   cudaError_t e = cudaMemcpyAsync(h->ctl + pl::kCtlEpoch, &epoch, sizeof epoch, cudaMemcpyHostToDevice,
@@ -816,6 +824,15 @@ purlin_status purlin_trace_enable(purlin_handle h, void* buffer, size_t buffer_b
   const size_t cap = (buffer_bytes - 8) / sizeof(pl::TraceRecord);
   h->trace = (unsigned long long*)buffer;
   h->trace_cap = (uint32_t)std::min<size_t>(cap, 0xFFFFFFFFu);
+  return PL_OK;
+}
+
+purlin_status purlin_workspace_query(purlin_handle h, size_t* bytes, int* grown) {
+  purlin_status st;
+  if ((st = check_handle(h))) return st;
+  std::lock_guard<std::mutex> lock(h->mu);
+  if (bytes) *bytes = h->ws_bytes;
+  if (grown) *grown = h->ws_grown;
   return PL_OK;
 }
 

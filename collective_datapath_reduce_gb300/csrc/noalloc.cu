@@ -49,6 +49,7 @@ struct NaArgs {
   uint32_t lag;              // rounds between a tile's reduce and its copies
   uint32_t slots;            // (tmax + lag) rounds of 2 * world slots
   uint32_t dst_coaligned;    // every output has the same address residue mod 16
+  uint32_t drop_notify;      // test hook: 1 + flag whose notify is skipped, or 0
 };
 
 // Wait for the flag to hold the launch's epoch.  A failure of this launch is
@@ -131,7 +132,7 @@ __global__ void __launch_bounds__(kNaThreads, 2) noalloc_kernel(const __grid_con
       }
     }
     __syncthreads();
-    if (threadIdx.x == 0 && s_kind == 1 && N > 1) {
+    if (threadIdx.x == 0 && s_kind == 1 && N > 1 && s_flag + 1 != a.drop_notify) {
       __threadfence();
       st_release(a.scratch + kNaCtlWords + s_flag, s_epoch);
     }
@@ -177,6 +178,9 @@ struct NaDevice {
 
 std::mutex g_na_mu;
 NaDevice g_na_dev[kNaMaxDevices];
+// Test hook (purlin_debug_noalloc_next): settings of the next call only.
+unsigned long long g_na_next_timeout_ns = 0;  // 0: the default
+uint32_t g_na_next_drop = 0;                  // 1 + flag whose notify is skipped, or 0
 
 // First call on a device: find the array's device address (host code only
 // holds a stand-in for it), zero it on the stream, and note the SM count.
@@ -210,6 +214,9 @@ purlin_status na_setup(int dev, cudaStream_t stream, NaDevice* out) {
 
 extern "C" purlin_status purlin_debug_noalloc_set_epoch(uint32_t epoch, purlin_stream_t stream) {
   using namespace pl;
+  // the counter holds the epoch the last launch used, 0 .. 0xFFFFFFFE: from
+  // 0xFFFFFFFF the next launch would take epoch 0, the value of cleared flags
+  if (epoch == 0xFFFFFFFFu) return PL_ERR_INVALID_ARG;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNaMaxDevices) {
     (void)cudaGetLastError();
@@ -229,6 +236,15 @@ extern "C" purlin_status purlin_debug_noalloc_set_epoch(uint32_t epoch, purlin_s
     (void)cudaGetLastError();
     return PL_ERR_CUDA;
   }
+  return PL_OK;
+}
+
+extern "C" purlin_status purlin_debug_noalloc_next(uint64_t timeout_ns, long long drop_tile) {
+  using namespace pl;
+  if (drop_tile >= (long long)kNaMaxFlags) return PL_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_na_mu);
+  g_na_next_timeout_ns = timeout_ns;
+  g_na_next_drop = drop_tile < 0 ? 0u : (uint32_t)drop_tile + 1u;
   return PL_OK;
 }
 
@@ -291,6 +307,13 @@ extern "C" purlin_status purlin_all_reduce_noalloc(int world, const void* const*
   a.scratch = d.scratch;
   a.device_status = device_status;
   a.timeout_ns = 2000000000ull;
+  {
+    std::lock_guard<std::mutex> lock(g_na_mu);
+    if (g_na_next_timeout_ns) a.timeout_ns = g_na_next_timeout_ns;
+    a.drop_notify = g_na_next_drop;
+    g_na_next_timeout_ns = 0;
+    g_na_next_drop = 0;
+  }
   a.q = q;
   a.rem = rem;
   a.elem = (uint32_t)E;

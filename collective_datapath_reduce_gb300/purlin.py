@@ -95,8 +95,10 @@ _SIGNATURES = {
     "purlin_debug_limit_buffer": (_i, [_vp, _i, _i, ctypes.c_uint64]),
     "purlin_debug_set_epoch": (_i, [_vp, ctypes.c_uint32, _vp]),
     "purlin_debug_noalloc_set_epoch": (_i, [ctypes.c_uint32, _vp]),
+    "purlin_debug_noalloc_next": (_i, [ctypes.c_uint64, ctypes.c_longlong]),
     "purlin_debug_drop_notify": (_i, [_vp, ctypes.c_longlong]),
     "purlin_query": (_i, [_vp, ctypes.POINTER(_i), ctypes.POINTER(_i), ctypes.POINTER(_i)]),
+    "purlin_workspace_query": (_i, [_vp, _SZP, ctypes.POINTER(_i)]),
     "purlin_all_reduce_noalloc": (_i, [_i, _PP, _PP, _sz, _i, _vp, _vp]),
     "purlin_trace_enable": (_i, [_vp, _vp, _sz]),
     "purlin_plan_describe": (_i, [_i, _i, _i, _SZP, ctypes.POINTER(ctypes.c_uint64),
@@ -313,6 +315,17 @@ def purlin_debug_noalloc_set_epoch(epoch: int, stream=None) -> int:
     return load().purlin_debug_noalloc_set_epoch(int(epoch), _stream(stream))
 
 
+def purlin_workspace_query(h):
+    """(status, workspace bytes, times the library grew it)."""
+    b, g = ctypes.c_size_t(), ctypes.c_int()
+    st = load().purlin_workspace_query(h, ctypes.byref(b), ctypes.byref(g))
+    return st, b.value, g.value
+
+
+def purlin_debug_noalloc_next(timeout_ns: int = 0, drop_tile: int = -1) -> int:
+    return load().purlin_debug_noalloc_next(int(timeout_ns), int(drop_tile))
+
+
 def purlin_trace_enable(h, buffer=None, buffer_bytes: int = 0) -> int:
     return load().purlin_trace_enable(h, _addr(buffer) or None, buffer_bytes)
 
@@ -335,8 +348,9 @@ def purlin_query(h):
     return st, a.value, b.value, c.value
 
 
-def purlin_plan_describe(coll, world, dtype, sizes, src_addr=None, dst_addr=None, sm_count=152, tune=None):
-    """Returns (status, items as dicts, grid, n_flags)."""
+def purlin_plan_describe(coll, world, dtype, sizes, src_addr=None, dst_addr=None, sm_count=152, tune=None,
+                         items=True):
+    """Returns (status, items as dicts, grid, n_flags); items=False skips the items."""
     lib = load()
     sz = _size_array(sizes)
     sa = (ctypes.c_uint64 * world)(*src_addr) if src_addr is not None else None
@@ -350,6 +364,8 @@ def purlin_plan_describe(coll, world, dtype, sizes, src_addr=None, dst_addr=None
                                   ctypes.byref(grid), ctypes.byref(nflags))
     if st != PL_OK:
         return st, [], 0, 0
+    if not items:
+        return st, [], grid.value, nflags.value
     arr = (purlin_item * max(1, n.value))()
     st = lib.purlin_plan_describe(coll, world, dtype, sz, sa, da, sm_count, tp, arr, n.value, ctypes.byref(n),
                                   ctypes.byref(grid), ctypes.byref(nflags))

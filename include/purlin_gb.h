@@ -60,6 +60,11 @@ extern "C" {
 #endif
 
 #define PURLIN_MAX_WORLD 16
+/* SNAC flags of the workspace the library allocates when purlin_initialize is
+ * given none (4 MiB of flags): the two-shot and ring AllReduce layouts at the
+ * tuning table's tile sizes for up to 8 ranks of about 9 GiB each, or 16
+ * ranks of about 4 GiB. */
+#define PURLIN_DEFAULT_WORKSPACE_FLAGS 1048576u
 
 typedef struct purlin_ctx* purlin_handle;
 typedef void* purlin_stream_t; /* a cudaStream_t */
@@ -99,14 +104,16 @@ typedef enum {
  * all_reduce_two_shot and all_reduce_ring).  One-shot: every byte range is
  * reduced once and the sum stored to all ranks.  Two-shot: rank o reduces
  * range o into its own output and notifies; a consumer then copies that range
- * to every other rank.  Both give the ascending-rank fold described above.
- * Ring: the classic ring -- chunk j's partial sum starts at rank j and each
- * hop adds the next rank's elements and stores the partial, in the data
- * type, to that rank's output; the finished chunks are then passed around
- * the ring.  Its results are deterministic but differ from the ascending fold:
- * each chunk is folded in its own rank order, and bf16 partials are rounded
- * at every hop (for fp32 with two ranks they are the same).  Only on request;
- * AUTO never picks it.  Register path only (PL_ERR_UNSUPPORTED otherwise). */
+ * to every other rank.  Ring: per tile, a running sum handed from rank to
+ * rank -- stage k adds rank k's elements to the sum the previous stage left
+ * in the outputs, each stage waiting for the previous one's flag -- then the
+ * finished tile is passed around the ring, output to output.  The running sum
+ * is kept in binary32 (for bf16 data as two 16-bit halves in two ranks'
+ * outputs) and every tile is walked from rank 0 upwards, so all three
+ * layouts give the ascending-rank fold described above, bit for bit.  The
+ * ring moves about three times the bytes of the one-shot layout; only on
+ * request, AUTO never picks it.  Register path only (PL_ERR_UNSUPPORTED
+ * otherwise). */
 typedef enum {
   PL_LAYOUT_AUTO = 0,
   PL_LAYOUT_ONE_SHOT = 1,
@@ -123,7 +130,8 @@ typedef struct {
   int unroll;       /* 16-byte vectors in flight per thread per source, 1..8 */
   int path;         /* 1 = register path, 2 = TMA bulk pipeline through shared memory */
   int chunk_bytes;  /* TMA stage size per source, or SNAC tile size of the two-shot and ring
-                       layouts (ring default: a 64th of a chunk, 64-128 KiB) */
+                       layouts (ring default: a 64th of bytes_per_rank / world, kept
+                       between 64 and 128 KiB) */
   int stages;       /* TMA pipeline depth, 2..8 */
   int store_hint;   /* 1 = default write-back stores, 2 = streaming (evict-first) stores */
   int min_cta_bytes;/* fewest work bytes given to one CTA before the grid shrinks */
@@ -159,7 +167,12 @@ typedef struct {
   uint64_t len;      /* bytes */
   uint32_t src_mask; /* bit r (r < 16): input of rank r; bit 16 + r: output of rank r.
                         Several bits = N-to-1 reduce in ascending bit order. */
-  uint32_t dst_mask; /* bit r: output of rank r */
+  uint32_t dst_mask; /* bit r (r < 16): output of rank r.  Bits 30 and 31 mark the ring
+                        layout's reduce items over bf16 data, whose running binary32 sum is
+                        kept as two 16-bit halves in two neighbouring ranks' outputs (low
+                        half in the lower rank): bit 30, the item's two output sources are
+                        those halves; bit 31, its two destinations receive the halves of
+                        the new sum instead of a rounded bf16 value. */
   uint32_t wait;     /* 0, or 1 + index of the SNAC flag consumed before the item */
   uint32_t notify;   /* 0, or 1 + index of the SNAC flag raised after the item */
   uint32_t cta;      /* CTA that runs the item; 0xFFFFFFFF under PL_SCHED_QUEUE (any CTA) */
@@ -177,9 +190,17 @@ size_t purlin_workspace_bytes(int world, size_t max_bytes_per_rank);
 /* Create a handle for `world` ranks on the current CUDA device (purlin 0.6.5,
  * "Host-side": create once, reuse for every collective).  `workspace` is
  * device memory owned by the caller, of `workspace_bytes` bytes, 256-byte
- * aligned; pass NULL to let the library allocate and grow its own.  The
- * workspace is zeroed on `stream` before the call returns.  On success *out
- * holds the handle. */
+ * aligned; it never grows, and a call whose plan needs more flags than it
+ * holds returns PL_ERR_WORKSPACE.  Pass NULL to let the library allocate its
+ * own: workspace_bytes, or PURLIN_DEFAULT_WORKSPACE_FLAGS flags if that is
+ * larger (size it with purlin_workspace_bytes for the largest call you will
+ * make).  A later call that needs more flags than a library-owned workspace
+ * holds grows it, once per growth: the call waits for `stream`, allocates a
+ * larger workspace, zeroes it and frees the old one (cudaMalloc and cudaFree
+ * may synchronise the whole device); under stream capture it returns
+ * PL_ERR_WORKSPACE instead.  purlin_workspace_query reports the size and the
+ * growths.  The workspace is zeroed on `stream` before the call returns.  On
+ * success *out holds the handle. */
 purlin_status purlin_initialize(int world, void* workspace, size_t workspace_bytes,
                                 purlin_stream_t stream, purlin_handle* out);
 
@@ -191,10 +212,9 @@ purlin_status purlin_finalize(purlin_handle h, purlin_stream_t stream);
 /* ----------------------------------------------------------- collectives */
 
 /* AllReduce (NKI all_reduce_hbm_kernel: sum tensors across ranks): dst[r][i] =
- * sum over s of src[s][i] for every r, folded as described at the top (the
- * ring layout folds in its own order; see purlin_layout).  bytes_per_rank =
- * size of each input and each output.  dtype PL_F32 or PL_BF16.  In-place
- * (src[r] == dst[r]) is allowed. */
+ * sum over s of src[s][i] for every r, folded as described at the top, in
+ * every layout (purlin_layout).  bytes_per_rank = size of each input and each
+ * output.  dtype PL_F32 or PL_BF16.  In-place (src[r] == dst[r]) is allowed. */
 purlin_status purlin_all_reduce(purlin_handle h, const void* const* src, void* const* dst,
                                 size_t bytes_per_rank, purlin_dtype dtype, purlin_mode mode,
                                 purlin_stream_t stream);
@@ -290,13 +310,24 @@ purlin_status purlin_debug_limit_buffer(purlin_handle h, int is_output, int rank
  * launch with SNAC flags used), in stream order.  Launches of SNAC plans use
  * epochs 1 .. 0xFFFFFFFF, one per launch, and flags are ready when they hold
  * the launch's epoch; the launch that used 0xFFFFFFFF clears every flag and
- * the counter starts again at 1.  Setting the counter near the end of the
- * cycle lets a test run that wrap without 2^32 launches.  Waits for the
- * stream; refused (PL_ERR_INVALID_ARG) while the stream is being captured. */
+ * publishes 0, and the counter starts again at 1.  Setting the counter near
+ * the end of the cycle lets a test run that wrap without 2^32 launches.  The
+ * counter only ever holds 0 .. 0xFFFFFFFE: 0xFFFFFFFF is refused
+ * (PL_ERR_INVALID_ARG; the next launch would take epoch 0, the value of a
+ * cleared flag, and its consumers would not wait).  Waits for the stream;
+ * refused (PL_ERR_INVALID_ARG) while the stream is being captured. */
 purlin_status purlin_debug_set_epoch(purlin_handle h, uint32_t epoch, purlin_stream_t stream);
 
 /* The same for purlin_all_reduce_noalloc's scratch on the current device. */
 purlin_status purlin_debug_noalloc_set_epoch(uint32_t epoch, purlin_stream_t stream);
+
+/* Test hook for purlin_all_reduce_noalloc: its next call (on any device) waits
+ * at most `timeout_ns` in each SNAC consume (0: the default 2 s) and skips the
+ * notify of the reduce of flag `drop_tile` (owner o's tile t is flag
+ * o x T + t, T = tiles of the largest owner range; -1: none), so a test can
+ * make a wait run out and read PL_ERR_TIMEOUT from its status word.  Applies
+ * to one call, then clears.  drop_tile >= 16384 returns PL_ERR_INVALID_ARG. */
+purlin_status purlin_debug_noalloc_next(uint64_t timeout_ns, long long drop_tile);
 
 /* Time limit of every SNAC consume wait, in nanoseconds (default 2e9). */
 purlin_status purlin_set_wait_timeout_ns(purlin_handle h, uint64_t ns);
@@ -315,6 +346,10 @@ purlin_status purlin_debug_drop_notify(purlin_handle h, long long item);
  * traced; records beyond the buffer's capacity are counted, not written.
  * NULL stops tracing. */
 purlin_status purlin_trace_enable(purlin_handle h, void* buffer, size_t buffer_bytes);
+
+/* Workspace of the handle: its size in bytes and how many times the library
+ * has grown it (always 0 for a caller's workspace).  Either pointer may be NULL. */
+purlin_status purlin_workspace_query(purlin_handle h, size_t* bytes, int* grown);
 
 /* Device facts the handle uses: SM count, compute capability (major*10+minor),
  * and the largest number of CTAs of the reduce kernel resident per SM. */
@@ -343,7 +378,10 @@ purlin_status purlin_query(purlin_handle h, int* sm_count, int* arch, int* max_c
  * elements -- about 1 GiB per rank; larger sizes return PL_ERR_WORKSPACE and
  * launch nothing.  device_status: NULL, or device memory the caller owns that
  * receives PL_OK or PL_ERR_TIMEOUT (a SNAC wait gave up after 2 s) when the
- * kernel ends.  Asynchronous on `stream`. */
+ * kernel ends.  A call that timed out leaves its outputs partly written; with
+ * a NULL device_status nothing reports it (the failure is kept only in the
+ * library's scratch, which no call reads back), so pass a status word
+ * wherever a time-out must be noticed.  Asynchronous on `stream`. */
 purlin_status purlin_all_reduce_noalloc(int world, const void* const* src, void* const* dst,
                                         size_t bytes_per_rank, purlin_dtype dtype, int* device_status,
                                         purlin_stream_t stream);

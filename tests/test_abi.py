@@ -62,3 +62,11 @@ def test_plan_rejects_bad_tune():
     assert st == P.PL_ERR_INVALID_ARG
     st, *_ = P.purlin_plan_describe(P.PL_COLL_ALL_GATHER, 2, P.PL_U8, [64], tune={"layout": 9})
     assert st == P.PL_ERR_UNSUPPORTED
+
+
+def test_noalloc_test_hook_is_host_only_and_checks_its_tile():
+    """purlin_debug_noalloc_next only records settings for the next call (no
+    GPU involved); a flag index past the scratch's 16384 flags is refused."""
+    assert P.purlin_debug_noalloc_next(1000, 16384) == P.PL_ERR_INVALID_ARG
+    assert P.purlin_debug_noalloc_next(1000, 3) == P.PL_OK
+    assert P.purlin_debug_noalloc_next(0, -1) == P.PL_OK      # cleared again
