@@ -18,6 +18,66 @@ def test_rejects_host_tensors_without_touching_the_library():
         purlin.all_gather(xs[:1], xs[:1], h)
 
 
+@pytest.fixture
+def no_library(monkeypatch):
+    """Any call into the C library fails the test: the checks must come first."""
+    from collective_datapath_reduce_gb300 import purlin as P
+
+    def boom(*a, **k):
+        raise AssertionError("the library was called")
+    for name in ("purlin_all_reduce", "purlin_reduce_scatter", "purlin_all_gather", "purlin_all_to_all",
+                 "purlin_all_gather_v", "purlin_all_to_all_v", "purlin_reduce_scatter_v"):
+        monkeypatch.setattr(P, name, boom)
+
+
+def _bad(fn, *args, match="bytes"):
+    with pytest.raises(ValueError, match=match):
+        fn(*args)
+
+
+def test_refuses_wrong_sized_or_typed_outputs_before_any_library_call(no_library):
+    """Each output must hold exactly what the collective writes (the C ABI
+    cannot see allocation sizes, so a short tensor would be overrun), in the
+    inputs' dtype."""
+    W = 4
+    h = purlin.Handle(raw=None, world=W, device=torch.device("cpu"))
+    f = lambda n, dt=torch.float32: [torch.zeros(n, dtype=dt) for _ in range(W)]
+    # AllReduce: outputs of the input size, inputs all one size
+    _bad(purlin.all_reduce, f(8), f(7), h)
+    _bad(purlin.all_reduce, f(8)[:3] + [torch.zeros(9)], f(8), h)
+    _bad(purlin.all_reduce, f(8), f(8, torch.bfloat16), h, match="dtype")
+    _bad(purlin.all_reduce, f(8, torch.int32), f(8, torch.int32), h, match="float32 or bfloat16")
+    # ReduceScatter: outputs of input / world elements
+    _bad(purlin.reduce_scatter, f(16), f(3), h)
+    _bad(purlin.reduce_scatter, f(16), f(16), h)
+    _bad(purlin.reduce_scatter, f(14), f(3), h, match="equal chunks")
+    _bad(purlin.reduce_scatter, f(16), f(4, torch.bfloat16), h, match="dtype")
+    # AllGather: outputs of world x input
+    _bad(purlin.all_gather, f(5), f(19), h)
+    _bad(purlin.all_gather, f(5), f(5), h)
+    # AllToAll: outputs of the input size
+    _bad(purlin.all_to_all, f(8), f(4), h)
+    _bad(purlin.all_to_all, f(6), f(6), h, match="equal chunks")
+    # AllGatherV: every output holds the sum of the inputs
+    xs = [torch.zeros(n) for n in (3, 0, 5, 1)]
+    _bad(purlin.all_gather_v, xs, f(8), h)
+    # AllToAllV: inputs hold their row sums, outputs their column sums
+    C = [[1, 0, 2, 0], [0, 0, 0, 3], [4, 0, 0, 0], [1, 1, 1, 1]]
+    rows = [torch.zeros(sum(r)) for r in C]
+    cols = [torch.zeros(sum(C[s][d] for s in range(W))) for d in range(W)]
+    _bad(purlin.all_to_all_v, rows, cols[:3] + [torch.zeros(1)], C, h)
+    _bad(purlin.all_to_all_v, rows[:3] + [torch.zeros(9)], cols, C, h)
+    _bad(purlin.all_to_all_v, rows, cols, [[1, 2]], h, match="counts")
+    # ReduceScatterV: every input holds the sum of counts, output r counts[r]
+    cnt = [2, 0, 3, 1]
+    _bad(purlin.reduce_scatter_v, f(6), [torch.zeros(c) for c in (2, 0, 3, 2)], cnt, h)
+    _bad(purlin.reduce_scatter_v, f(7), [torch.zeros(c) for c in cnt], cnt, h)
+    # right sizes: the only complaint left is that host tensors are not pinned
+    _bad(purlin.all_to_all_v, rows, cols, C, h, match="pinned")
+    _bad(purlin.reduce_scatter_v, f(6), [torch.zeros(c) for c in cnt], cnt, h, match="pinned")
+    _bad(purlin.all_gather, f(5), f(20), h, match="pinned")
+
+
 @pytest.mark.gpu
 def test_torch_front_end_matches_oracle():
     dev = torch.device("cuda", 0)
