@@ -70,9 +70,8 @@ def workloads(P, inputs):
                  [S] * WORLD, lambda h, s, d, st: P.purlin_all_reduce(h, s, d, S, P.PL_BF16, 0, st),
                  ALGO_BYTES, P.PL_COLL_ALL_REDUCE, S, tune={"layout": P.PL_LAYOUT_TWO_SHOT}),
         Workload("allreduce_ring_bf16_8x64MiB", WORKLOAD.replace("AllReduce sum", "AllReduce sum, ring layout "
-                 "(each chunk's partial sum passes rank to rank, rounded to bf16 at every hop, then the "
-                 "finished chunks pass around the ring: 2(N-1) SNAC stages per tile),", 1).replace(
-                 "fp32 ascending-rank accumulation", "fp32 adds in ring order"), "bf16",
+                 "(per tile a binary32 running sum handed from rank to rank in ascending order, then the "
+                 "finished tile passed around the ring: 2(N-1) SNAC stages per tile),", 1), "bf16",
                  lambda: list(inputs.w2_allreduce_bf16(WORLD, N_ELEMS, seed=1)),
                  [S] * WORLD, lambda h, s, d, st: P.purlin_all_reduce(h, s, d, S, P.PL_BF16, 0, st),
                  ALGO_BYTES, P.PL_COLL_ALL_REDUCE, S, tune={"layout": P.PL_LAYOUT_RING}),
@@ -333,7 +332,7 @@ def run_own(args, dist):
     host_out = [torch.empty(b, dtype=torch.uint8).pin_memory() for b in wl.out_bytes]
     in_bytes = sum(t.numel() for t in host_in)
     out_bytes = sum(wl.out_bytes)
-    Ke = max(3, min(K, 20, int((4 << 30) // max(in_bytes + out_bytes, 1))))
+    Ke = K                                           # as many steps as the device-timed region
     src2 = [torch.empty_like(t) for t in src]
     dst2 = [torch.empty_like(t) for t in dst]
     sets = [([t.data_ptr() for t in src], [t.data_ptr() for t in dst], src, dst),
@@ -428,19 +427,16 @@ def run_own(args, dist):
     P.check(P.purlin_finalize(h, stream), "purlin_finalize")
 
     cpu = None
-    if headline and dist.rank == 0 and dist.world == 1 and not args.no_cpu:
-        cpu = cpu_baseline(np.stack(x), budget_s=12.0)
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(wl, x, budget_s=12.0)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-        "config": {"workload": wl.desc, "name": wl.name, "world": WORLD,
-                   "algorithmic_bytes_per_step": wl.algo_bytes,
-                   "parallelism": f"replicas{dist.world}" if dist.world > 1 else "single-gpu",
-                   "l2": f"inputs {in_bytes >> 20} MiB and outputs {out_bytes >> 20} MiB per step exceed the "
-                         "126 MiB L2; no flush",
-                   "tune": tune},
+        "config": config_of(wl, x),
+        "parallelism": f"replicas{dist.world}" if dist.world > 1 else "single-gpu",
+        "tune": tune,
         "roofline": roofline, "e2e": e2e, "gpu_launches": K, "clocks": clk,
         "cpu_baseline": cpu,
         "pct_of_hbm_peak": round(100 * value / dist.world / peak, 2),
@@ -558,12 +554,17 @@ def side_table(P, h, stream, dev):
         out["all_reduce_bf16"][key] = point(2 * WORLD * size, timeit(
             lambda: chk(P.purlin_all_reduce(h, x, y, size, P.PL_BF16, 0, stream))), size)
         if size >= 16 * MI:
+            one_shot = [t.clone() for t in y]
             for layout, name in ((P.PL_LAYOUT_TWO_SHOT, "all_reduce_two_shot_bf16"),
                                  (P.PL_LAYOUT_RING, "all_reduce_ring_bf16")):
                 P.check(P.purlin_tune_override(h, {"layout": layout}))
+                for t in y:
+                    t.fill_(float("nan"))
                 out[name][key] = point(2 * WORLD * size, timeit(
                     lambda: chk(P.purlin_all_reduce(h, x, y, size, P.PL_BF16, 0, stream))), size)
+                out[name][key]["max_ulp_vs_one_shot"] = max_ulp_dev(y, one_shot, stream)
             P.check(P.purlin_tune_override(h, None))
+            del one_shot
         del x, y
         x = bufs(size // 4, WORLD, torch.float32)
         y = [torch.empty(size // 4 // WORLD, dtype=torch.float32, device=dev) for _ in range(WORLD)]
@@ -578,11 +579,15 @@ def side_table(P, h, stream, dev):
     for size in (16 * MI, 64 * MI, 256 * MI):
         x = bufs(size // 2, WORLD, torch.bfloat16)
         y = [torch.empty_like(t) for t in x]
-        out["all_reduce_noalloc_bf16"][f"{size >> 20}MiB"] = point(2 * WORLD * size, timeit(
+        one_shot = [torch.empty_like(t) for t in x]
+        chk(P.purlin_all_reduce(h, x, one_shot, size, P.PL_BF16, 0, stream))
+        key = f"{size >> 20}MiB"
+        out["all_reduce_noalloc_bf16"][key] = point(2 * WORLD * size, timeit(
             lambda: chk(P.purlin_all_reduce_noalloc(WORLD, x, y, size, P.PL_BF16, dstat, stream)), graph=False), size)
         if int(dstat.item()) != 0:
             raise RuntimeError("allocation-free AllReduce reported a device error")
-        del x, y
+        out["all_reduce_noalloc_bf16"][key]["max_ulp_vs_one_shot"] = max_ulp_dev(y, one_shot, stream)
+        del x, y, one_shot
     torch.cuda.empty_cache()
     # ReduceScatterV: uneven chunks (workload 5's first row of counts), bf16
     from collective_datapath_reduce_gb300 import inputs as _inputs
@@ -643,34 +648,57 @@ def side_table(P, h, stream, dev):
     return out
 
 
+def max_ulp_dev(got, want, stream):
+    """Largest ulp distance between two lists of bf16 tensors, on the device:
+    bit patterns folded to ordered integers (negative values to minus their
+    magnitude bits), then the largest difference.  0 = bit-identical."""
+    import torch
+    m = 0
+    with torch.cuda.stream(stream):
+        for g, w in zip(got, want):
+            a = g.view(torch.int16).to(torch.int32)
+            b = w.view(torch.int16).to(torch.int32)
+            a = torch.where(a < 0, -(a & 0x7FFF), a)
+            b = torch.where(b < 0, -(b & 0x7FFF), b)
+            m = max(m, int((a - b).abs().max().item()))
+    return m
+
+
 # ---------------------------------------------------------- CPU baseline
 
-def _oracle_sample(x, n_sample):
-    import oracle
-    ins = [x[r, :n_sample] for r in range(x.shape[0])]
-    t0 = time.perf_counter()
-    oracle.all_reduce(ins, "bf16")
-    return time.perf_counter() - t0
+def config_of(wl, x):
+    """The workload a line measures (identical in both arms): what it is, its
+    size, and how its working set compares with the GPU's L2."""
+    in_bytes = sum(int(np.asarray(a).nbytes) for a in x)
+    out_bytes = sum(wl.out_bytes)
+    return {"workload": wl.desc, "name": wl.name, "world": WORLD, "algorithmic_bytes_per_step": wl.algo_bytes,
+            "l2": f"inputs {in_bytes >> 20} MiB and outputs {out_bytes >> 20} MiB per step exceed the 126 MiB "
+                  "L2; no flush between steps"}
 
 
-def cpu_baseline(x, budget_s=12.0):
-    """The CPU oracle, as it stands, on a bounded sample of the workload."""
-    n = 1 << 20
-    t = _oracle_sample(x, n)
-    n_sample = int(min(x.shape[1], max(n, n * (budget_s / 4) / max(t, 1e-3))))
-    n_sample -= n_sample % 8
-    reps, spent = 0, 0.0
-    while spent < budget_s and reps < 50:
-        spent += _oracle_sample(x, n_sample)
-        reps += 1
-    per = spent / reps
-    nbytes = 2 * x.shape[0] * n_sample * ELEM
-    return {"value": round(nbytes / per / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {n_sample} of {x.shape[1]} elements of each of the {x.shape[0]} ranks, "
-                      f"{reps} runs, {per:.3f} s each (numpy, single-threaded)"}
+def host_cpu():
+    """Core count and CPU model of this host (lscpu, else /proc/cpuinfo)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().startswith("Model name:"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for ln in f:
+                    if ln.lower().startswith(("model name", "cpu model")):
+                        model = ln.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    import platform
+    return {"host_cores": os.cpu_count(), "cpu_model": model or platform.machine()}
 
-
-# ----------------------------------------------------------- reference arm
 
 def _reference_call(name):
     """The oracle function of a workload: f(list of rank arrays) -> outputs."""
@@ -680,7 +708,7 @@ def _reference_call(name):
     return {
         "allreduce_bf16_8x64MiB": lambda ins: oracle.all_reduce(ins, "bf16"),
         "allreduce_two_shot_bf16_8x64MiB": lambda ins: oracle.all_reduce(ins, "bf16"),
-        "allreduce_ring_bf16_8x64MiB": lambda ins: oracle.all_reduce_ring(ins, "bf16"),
+        "allreduce_ring_bf16_8x64MiB": lambda ins: oracle.all_reduce(ins, "bf16"),
         "reduce_scatter_f32_8x256MiB": lambda ins: oracle.reduce_scatter(ins, "f32"),
         "reduce_scatter_bf16_8x128MiB": lambda ins: oracle.reduce_scatter(ins, "bf16"),
         "all_gather_u8_8x256MiB": oracle.all_gather,
@@ -689,6 +717,58 @@ def _reference_call(name):
         "all_gather_v_bf16_w5": lambda ins: oracle.all_gather_v(ins, [int(v) for v in c5]),
     }[name]
 
+
+class OracleRun:
+    """The workload's oracle, as it stands, on a bounded sample: the first
+    `k` elements of every rank (whole chunks for ReduceScatter / AllToAll), or
+    the whole workload for the V collectives, whose counts fix the layout.
+    A run's throughput counts the sample's share of the algorithmic bytes."""
+
+    def __init__(self, wl, x, run_budget_s):
+        self.fn = _reference_call(wl.name)
+        self.x = [np.asarray(a) for a in x]
+        self.algo_bytes = wl.algo_bytes
+        if wl.name.endswith("_w5"):
+            self.k, self.frac = None, 1.0
+        else:
+            n = self.x[0].size
+            probe = min(n, 1 << 20)
+            probe -= probe % (8 * WORLD)
+            t = self.run_once(probe)
+            k = int(min(n, max(1 << 16, probe * run_budget_s / max(t, 1e-4))))
+            self.k = k - k % (8 * WORLD)
+            self.frac = self.k / n
+
+    def run_once(self, k=None):
+        k = self.k if k is None else k
+        ins = self.x if k is None else [a[:k] for a in self.x]
+        t0 = time.perf_counter()
+        self.fn(ins)
+        return time.perf_counter() - t0
+
+    def gbs(self, seconds):
+        return self.algo_bytes * self.frac / seconds / 1e9
+
+    def sample(self):
+        what = ("the whole workload per run" if self.k is None else
+                f"first {self.k} of {self.x[0].size} elements of each of the {WORLD} ranks per run")
+        return what + " (numpy, single-threaded)"
+
+
+def cpu_baseline(wl, x, budget_s=12.0):
+    """The CPU oracle of the workload, as it stands, for about budget_s seconds."""
+    o = OracleRun(wl, x, run_budget_s=budget_s / 8)
+    reps, spent = 0, 0.0
+    while spent < budget_s and reps < 50:
+        spent += o.run_once()
+        reps += 1
+    per = spent / reps
+    return dict({"value": round(o.gbs(per), 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                 "sample": f"{o.sample()}, {reps} runs, {per:.3f} s each",
+                 "sampled_fraction": round(o.frac, 6)}, **host_cpu())
+
+
+# ----------------------------------------------------------- reference arm
 
 def run_reference(args, dist):
     """The oracle of the selected workload times itself on the host cores, on
@@ -699,44 +779,22 @@ def run_reference(args, dist):
     from collective_datapath_reduce_gb300 import inputs
     from collective_datapath_reduce_gb300 import purlin as P  # names only: the library is not loaded
     wl = workloads(P, inputs)[args.workload]
-    fn = _reference_call(wl.name)
     x = [np.asarray(a) for a in wl.make_inputs()]
-    full = sum(a.size for a in x)
-    if wl.name.endswith("_w5"):
-        def run(_k):
-            t0 = time.perf_counter()
-            fn(x)
-            return time.perf_counter() - t0
-        k_sample, frac = None, 1.0
-    else:
-        def run(k):
-            ins = [a[:k] for a in x]
-            t0 = time.perf_counter()
-            fn(ins)
-            return time.perf_counter() - t0
-        n = x[0].size
-        probe = min(n, 1 << 20)
-        t = run(probe - probe % (8 * WORLD))
-        steps = args.steps + args.warmup
-        per_step_budget = max(0.05, 120.0 / max(steps, 1))
-        k_sample = int(min(n, max(1 << 16, probe * per_step_budget / max(t, 1e-4))))
-        k_sample -= k_sample % (8 * WORLD)            # whole chunks for ReduceScatter / AllToAll
-        frac = k_sample / n
+    steps = args.steps + args.warmup
+    o = OracleRun(wl, x, run_budget_s=max(0.05, 120.0 / max(steps, 1)))
     for _ in range(args.warmup):
-        run(k_sample)
-    times = [run(k_sample) for _ in range(args.steps)]
+        o.run_once()
+    times = [o.run_once() for _ in range(args.steps)]
     per = sum(times) / len(times)
-    value = round(wl.algo_bytes * frac / per / 1e9, 4)
-    sample = ("the whole workload per step" if k_sample is None else
-              f"first {k_sample} of {x[0].size} elements of each of the {WORLD} ranks per step") + \
-        " (numpy, single-threaded)"
+    value = round(o.gbs(per), 4)
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-        "config": {"workload": wl.desc, "name": wl.name, "world": WORLD, "algorithmic_bytes_per_step": wl.algo_bytes,
-                   "sampled_fraction": round(frac, 6), "input_elements": full},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "config": config_of(wl, x),
+        "sampled_fraction": round(o.frac, 6), "input_elements": sum(a.size for a in x),
+        "cpu_baseline": dict({"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                              "sample": o.sample()}, **host_cpu()),
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }), flush=True)

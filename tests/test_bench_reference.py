@@ -27,6 +27,9 @@ def _check_line(d, n_gpus):
     assert d["config"]["name"] == WORKLOAD
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["host_cores"] == os.cpu_count() and d["cpu_baseline"]["cpu_model"]
+    # the workload only: the own arm prints the same object (see below)
+    assert set(d["config"]) == {"workload", "name", "world", "algorithmic_bytes_per_step", "l2"}
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
 
 
@@ -51,3 +54,17 @@ def test_reference_arm_two_ranks_prints_once():
     lines = _lines(r.stdout)
     assert len(lines) == 1
     _check_line(lines[0], 2)
+
+
+def test_both_arms_describe_the_workload_alike():
+    """The own arm and the reference arm build `config` with one function from
+    the workload alone, so the two lines of a workload carry equal objects."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from collective_datapath_reduce_gb300 import inputs
+    from collective_datapath_reduce_gb300 import purlin as P
+    wl = bench.workloads(P, inputs)[WORKLOAD]
+    x = wl.make_inputs()
+    import numpy as np
+    a, b = bench.config_of(wl, x), bench.config_of(wl, [np.copy(v) for v in x])
+    assert a == b and a["name"] == WORKLOAD and "MiB" in a["l2"]
