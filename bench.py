@@ -54,10 +54,13 @@ class Workload:
         self.tune = tune  # tuning override applied to the handle (None: the table's choice)
 
 
-def workloads(P, inputs):
-    """The five workloads' largest single-GPU cases (the first is the headline)."""
+def workloads(P, inputs, w4_mib=256):
+    """The five workloads' largest single-GPU cases (the first is the headline).
+    w4_mib: per-rank size of the AllGather / AllToAll byte workloads (256 MiB;
+    smaller only for profiler captures, which must stay a few GB)."""
     MI = 1 << 20
     C5, c5 = inputs.w5_counts(WORLD)
+    G = w4_mib * MI
     w = [
         Workload("allreduce_bf16_8x64MiB", WORKLOAD, "bf16",
                  lambda: list(inputs.w2_allreduce_bf16(WORLD, N_ELEMS, seed=1)),
@@ -71,7 +74,7 @@ def workloads(P, inputs):
                  ALGO_BYTES, P.PL_COLL_ALL_REDUCE, S, tune={"layout": P.PL_LAYOUT_TWO_SHOT}),
         Workload("allreduce_ring_bf16_8x64MiB", WORKLOAD.replace("AllReduce sum", "AllReduce sum, ring layout "
                  "(per tile a binary32 running sum handed from rank to rank in ascending order, then the "
-                 "finished tile passed around the ring: 2(N-1) SNAC stages per tile),", 1), "bf16",
+                 "finished tile passed around the ring: 2(N-1) SNAC stages per tile)", 1), "bf16",
                  lambda: list(inputs.w2_allreduce_bf16(WORLD, N_ELEMS, seed=1)),
                  [S] * WORLD, lambda h, s, d, st: P.purlin_all_reduce(h, s, d, S, P.PL_BF16, 0, st),
                  ALGO_BYTES, P.PL_COLL_ALL_REDUCE, S, tune={"layout": P.PL_LAYOUT_RING}),
@@ -85,14 +88,14 @@ def workloads(P, inputs):
                  lambda: list(inputs.w3_reduce_scatter(WORLD, 64 * MI, seed=2, dtype="bf16")),
                  [16 * MI] * WORLD, lambda h, s, d, st: P.purlin_reduce_scatter(h, s, d, 128 * MI, P.PL_BF16, 0, st),
                  WORLD * 128 * MI + 128 * MI, P.PL_COLL_REDUCE_SCATTER, 128 * MI),
-        Workload("all_gather_u8_8x256MiB", "AllGather, 8 ranks, uint8 payload, 256 MiB per rank, seed 3", "u8",
-                 lambda: list(inputs.w4_bytes(WORLD, 256 * MI)),
-                 [WORLD * 256 * MI] * WORLD, lambda h, s, d, st: P.purlin_all_gather(h, s, d, 256 * MI, st),
-                 WORLD * 256 * MI * (1 + WORLD), P.PL_COLL_ALL_GATHER, 256 * MI),
-        Workload("all_to_all_u8_8x256MiB", "AllToAll, 8 ranks, uint8 payload, 256 MiB per rank, seed 3", "u8",
-                 lambda: list(inputs.w4_bytes(WORLD, 256 * MI)),
-                 [256 * MI] * WORLD, lambda h, s, d, st: P.purlin_all_to_all(h, s, d, 256 * MI, st),
-                 2 * WORLD * 256 * MI, P.PL_COLL_ALL_TO_ALL, 256 * MI),
+        Workload("all_gather_u8_8x256MiB", f"AllGather, 8 ranks, uint8 payload, {w4_mib} MiB per rank, seed 3", "u8",
+                 lambda: list(inputs.w4_bytes(WORLD, G)),
+                 [WORLD * G] * WORLD, lambda h, s, d, st: P.purlin_all_gather(h, s, d, G, st),
+                 WORLD * G * (1 + WORLD), P.PL_COLL_ALL_GATHER, G),
+        Workload("all_to_all_u8_8x256MiB", f"AllToAll, 8 ranks, uint8 payload, {w4_mib} MiB per rank, seed 3", "u8",
+                 lambda: list(inputs.w4_bytes(WORLD, G)),
+                 [G] * WORLD, lambda h, s, d, st: P.purlin_all_to_all(h, s, d, G, st),
+                 2 * WORLD * G, P.PL_COLL_ALL_TO_ALL, G),
         Workload("all_to_all_v_bf16_w5",
                  "AllToAllV, 8 ranks, bf16 N(0,1), counts uniform in [0, 4 Mi] elements with forced zeros and "
                  "counts not multiple of 8, seed 4", "bf16",
@@ -120,7 +123,17 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--workload", default="allreduce_bf16_8x64MiB",
                     help="which collective to time (default: the AllReduce headline)")
-    return ap.parse_args()
+    ap.add_argument("--device-only", action="store_true",
+                    help="time the device leg only: no end-to-end legs, side table or CPU baseline "
+                         "(profiler captures: few launches, little memory)")
+    ap.add_argument("--tune", default="",
+                    help="tuning fields over the workload's own, e.g. store_hint=3,snac_lag=2")
+    ap.add_argument("--w4-mib", type=int, default=256,
+                    help="per-rank MiB of the AllGather / AllToAll workloads (smaller for profiler captures)")
+    args = ap.parse_args()
+    if args.device_only:
+        args.no_extras = args.no_cpu = True
+    return args
 
 
 # ------------------------------------------------------------ distributed
@@ -262,8 +275,10 @@ def run_own(args, dist):
     torch.cuda.set_device(dev)
     dist.init("nccl")
     stream = torch.cuda.Stream(device=dev)
-    wl = workloads(P, inputs)[args.workload]
+    wl = workloads(P, inputs, args.w4_mib)[args.workload]
     headline = args.workload == "allreduce_bf16_8x64MiB"
+    if args.tune:
+        wl.tune = dict(wl.tune or {}, **{k: int(v) for k, v in (f.split("=") for f in args.tune.split(","))})
 
     x = wl.make_inputs()                                      # host arrays, one per rank
     host_in = [torch.from_numpy(np.ascontiguousarray(a).view(np.uint8)).pin_memory() for a in x]
@@ -325,92 +340,94 @@ def run_own(args, dist):
     ms_per_step = total_ms / K
     value = dist.world * wl.algo_bytes * K / (total_ms / 1e3) / 1e9
 
-    # End to end: every step copies its inputs in from pinned host memory, runs
-    # the collective and copies its outputs back.  Steps are pipelined over three
-    # streams and two device buffer sets, so the host->device copy of step k+1
-    # and the device->host copy of step k-1 overlap the kernel of step k.
-    host_out = [torch.empty(b, dtype=torch.uint8).pin_memory() for b in wl.out_bytes]
-    in_bytes = sum(t.numel() for t in host_in)
-    out_bytes = sum(wl.out_bytes)
-    Ke = K                                           # as many steps as the device-timed region
-    src2 = [torch.empty_like(t) for t in src]
-    dst2 = [torch.empty_like(t) for t in dst]
-    sets = [([t.data_ptr() for t in src], [t.data_ptr() for t in dst], src, dst),
-            ([t.data_ptr() for t in src2], [t.data_ptr() for t in dst2], src2, dst2)]
-    # Each direction's per-rank copies are spread over NC streams, so several
-    # copy engines work at once.
-    NC = 4
-    s_in = [torch.cuda.Stream(device=dev) for _ in range(NC)]
-    s_out = [torch.cuda.Stream(device=dev) for _ in range(NC)]
-    ev_in = [[torch.cuda.Event() for _ in range(NC)] for _ in range(Ke)]
-    ev_done = [torch.cuda.Event() for _ in range(Ke)]
-    ev_out = [[torch.cuda.Event() for _ in range(NC)] for _ in range(Ke)]
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    dist.barrier()
-    torch.cuda.synchronize(dev)
-    e0.record(stream)
-    for q in s_in + s_out:
-        q.wait_stream(stream)
-    for k in range(Ke):
-        sp, dp, sb, db = sets[k % 2]
-        for c, q in enumerate(s_in):
-            with torch.cuda.stream(q):
+    e2e = None
+    if not args.device_only:
+        # End to end: every step copies its inputs in from pinned host memory, runs
+        # the collective and copies its outputs back.  Steps are pipelined over three
+        # streams and two device buffer sets, so the host->device copy of step k+1
+        # and the device->host copy of step k-1 overlap the kernel of step k.
+        host_out = [torch.empty(b, dtype=torch.uint8).pin_memory() for b in wl.out_bytes]
+        in_bytes = sum(t.numel() for t in host_in)
+        out_bytes = sum(wl.out_bytes)
+        Ke = K                                           # as many steps as the device-timed region
+        src2 = [torch.empty_like(t) for t in src]
+        dst2 = [torch.empty_like(t) for t in dst]
+        sets = [([t.data_ptr() for t in src], [t.data_ptr() for t in dst], src, dst),
+                ([t.data_ptr() for t in src2], [t.data_ptr() for t in dst2], src2, dst2)]
+        # Each direction's per-rank copies are spread over NC streams, so several
+        # copy engines work at once.
+        NC = 4
+        s_in = [torch.cuda.Stream(device=dev) for _ in range(NC)]
+        s_out = [torch.cuda.Stream(device=dev) for _ in range(NC)]
+        ev_in = [[torch.cuda.Event() for _ in range(NC)] for _ in range(Ke)]
+        ev_done = [torch.cuda.Event() for _ in range(Ke)]
+        ev_out = [[torch.cuda.Event() for _ in range(NC)] for _ in range(Ke)]
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        dist.barrier()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for q in s_in + s_out:
+            q.wait_stream(stream)
+        for k in range(Ke):
+            sp, dp, sb, db = sets[k % 2]
+            for c, q in enumerate(s_in):
+                with torch.cuda.stream(q):
+                    if k >= 2:
+                        q.wait_event(ev_done[k - 2])      # step k-2 has finished reading this input set
+                    for r in range(c, WORLD, NC):
+                        if host_in[r].numel():
+                            sb[r][:host_in[r].numel()].copy_(host_in[r], non_blocking=True)
+                    ev_in[k][c].record(q)
+            for c in range(NC):
+                stream.wait_event(ev_in[k][c])
                 if k >= 2:
-                    q.wait_event(ev_done[k - 2])      # step k-2 has finished reading this input set
-                for r in range(c, WORLD, NC):
-                    if host_in[r].numel():
-                        sb[r][:host_in[r].numel()].copy_(host_in[r], non_blocking=True)
-                ev_in[k][c].record(q)
-        for c in range(NC):
-            stream.wait_event(ev_in[k][c])
-            if k >= 2:
-                stream.wait_event(ev_out[k - 2][c])   # step k-2's outputs have reached the host
-        st = wl.call(h, sp, dp, stream)
-        if st != P.PL_OK:
-            raise P.PurlinError(st, wl.name)
-        ev_done[k].record(stream)
-        for c, q in enumerate(s_out):
-            with torch.cuda.stream(q):
-                q.wait_event(ev_done[k])
-                for r in range(c, WORLD, NC):
-                    if wl.out_bytes[r]:
-                        host_out[r].copy_(db[r][:wl.out_bytes[r]], non_blocking=True)
-                ev_out[k][c].record(q)
-    for q in s_in + s_out:
-        stream.wait_stream(q)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    dist.barrier()
-    e2e_ms = dist.max(e0.elapsed_time(e1), dev) / Ke
-    staged = {"value": round(dist.world * wl.algo_bytes / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
-              "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes, "ms_per_step": round(e2e_ms, 4),
-              "steps": Ke, "method": "staged: copy-engine copies in and out, h2d(k+1) and d2h(k-1) overlap the "
-              "kernel of step k; 4 copy streams per direction, 2 buffer sets"}
-    del src2, dst2
+                    stream.wait_event(ev_out[k - 2][c])   # step k-2's outputs have reached the host
+            st = wl.call(h, sp, dp, stream)
+            if st != P.PL_OK:
+                raise P.PurlinError(st, wl.name)
+            ev_done[k].record(stream)
+            for c, q in enumerate(s_out):
+                with torch.cuda.stream(q):
+                    q.wait_event(ev_done[k])
+                    for r in range(c, WORLD, NC):
+                        if wl.out_bytes[r]:
+                            host_out[r].copy_(db[r][:wl.out_bytes[r]], non_blocking=True)
+                    ev_out[k][c].record(q)
+        for q in s_in + s_out:
+            stream.wait_stream(q)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        dist.barrier()
+        e2e_ms = dist.max(e0.elapsed_time(e1), dev) / Ke
+        staged = {"value": round(dist.world * wl.algo_bytes / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+                  "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes, "ms_per_step": round(e2e_ms, 4),
+                  "steps": Ke, "method": "staged: copy-engine copies in and out, h2d(k+1) and d2h(k-1) overlap the "
+                  "kernel of step k; 4 copy streams per direction, 2 buffer sets"}
+        del src2, dst2
 
-    # End to end in place: the call is given the pinned host buffers themselves
-    # and its kernel reads the inputs from host memory and writes the outputs
-    # to host memory over the host link (the same bytes cross it each step).
-    hp_in = [t.data_ptr() if t.numel() else None for t in host_in]
-    hp_out = [t.data_ptr() if t.numel() else None for t in host_out]
-    P.check(wl.call(h, hp_in, hp_out, stream), wl.name)   # builds the host-memory plan
-    stream.synchronize()
-    z0 = torch.cuda.Event(enable_timing=True)
-    z1 = torch.cuda.Event(enable_timing=True)
-    dist.barrier()
-    torch.cuda.synchronize(dev)
-    z0.record(stream)
-    for _ in range(Ke):
-        P.check(wl.call(h, hp_in, hp_out, stream), wl.name)
-    z1.record(stream)
-    torch.cuda.synchronize(dev)
-    dist.barrier()
-    zc_ms = dist.max(z0.elapsed_time(z1), dev) / Ke
-    e2e = {"value": round(dist.world * wl.algo_bytes / (zc_ms / 1e3) / 1e9, 2), "unit": "GB/s",
-           "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes, "ms_per_step": round(zc_ms, 4),
-           "steps": Ke, "method": "in place: the C-ABI call takes the pinned host buffers, its kernel reads the "
-           "inputs from host memory and writes the results to host memory", "staged": staged}
+        # End to end in place: the call is given the pinned host buffers themselves
+        # and its kernel reads the inputs from host memory and writes the outputs
+        # to host memory over the host link (the same bytes cross it each step).
+        hp_in = [t.data_ptr() if t.numel() else None for t in host_in]
+        hp_out = [t.data_ptr() if t.numel() else None for t in host_out]
+        P.check(wl.call(h, hp_in, hp_out, stream), wl.name)   # builds the host-memory plan
+        stream.synchronize()
+        z0 = torch.cuda.Event(enable_timing=True)
+        z1 = torch.cuda.Event(enable_timing=True)
+        dist.barrier()
+        torch.cuda.synchronize(dev)
+        z0.record(stream)
+        for _ in range(Ke):
+            P.check(wl.call(h, hp_in, hp_out, stream), wl.name)
+        z1.record(stream)
+        torch.cuda.synchronize(dev)
+        dist.barrier()
+        zc_ms = dist.max(z0.elapsed_time(z1), dev) / Ke
+        e2e = {"value": round(dist.world * wl.algo_bytes / (zc_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes, "ms_per_step": round(zc_ms, 4),
+               "steps": Ke, "method": "in place: the C-ABI call takes the pinned host buffers, its kernel reads the "
+               "inputs from host memory and writes the results to host memory", "staged": staged}
 
     peak, peak_kind = measured_peaks()
     achieved = wl.algo_bytes / (kernel_ms / 1e3) / 1e9

@@ -108,6 +108,11 @@ const void* pick_kernel(const pl::Plan& p) {
     u = u >= 8 ? 8 : u >= 4 ? 4 : u >= 2 ? 2 : 1;
     return pl::kernel_copy(u);
   }
+  if (p.tune.store_hint == 3) {
+    if (p.dtype == pl::kF32) return pl::kernel_reduce_l2_f32(p.nsrc, p.tune.unroll);
+    if (p.dtype == pl::kBF16) return pl::kernel_reduce_l2_bf16(p.nsrc, p.tune.unroll);
+    return nullptr;
+  }
   if (p.tune.layout == pl::kRing && p.sync) {
     if (p.dtype == pl::kF32) return pl::kernel_reduce_ring_f32(p.tune.unroll);
     if (p.dtype == pl::kBF16) return pl::kernel_reduce_ring_bf16(p.tune.unroll);
@@ -469,11 +474,19 @@ size_t purlin_workspace_bytes(int world, size_t max_bytes_per_rank) {
   // flags of the SNAC AllReduce layouts at the table's tile size, for the
   // smallest element (bf16): one per tile of each rank's share (two-shot), or
   // one per tile and stage but the last of 2 (world - 1) stages (ring)
-  const pl::Tune t = pl::tune_table(pl::kAllReduce, world, pl::kBF16, max_bytes_per_rank);
-  const uint64_t per_owner = (max_bytes_per_rank / 2 + (uint64_t)world - 1) / (uint64_t)world * 2;
-  const uint64_t tiles = std::max<uint64_t>(1, (per_owner + (uint64_t)t.chunk_bytes - 1) / (uint64_t)t.chunk_bytes);
+  const uint64_t S = max_bytes_per_rank;
+  const pl::Tune t = pl::tune_table(pl::kAllReduce, world, pl::kBF16, S);
+  // ring: its tiles are a 64th of a rank's share, at least 64 KiB
+  const pl::Tune tr = pl::resolve_tune(pl::kAllReduce, pl::kAllReduce, world, pl::kBF16, S,
+                                       [] { pl::Tune o; o.layout = pl::kRing; return o; }());
+  const uint64_t per_owner = (S / 2 + (uint64_t)world - 1) / (uint64_t)world * 2;
+  const uint64_t ring_tiles = std::max<uint64_t>(1, (per_owner + (uint64_t)tr.chunk_bytes - 1) / (uint64_t)tr.chunk_bytes);
   const uint64_t per_tile = world > 1 ? 2 * (uint64_t)world - 3 : 1;
-  return (size_t)pl::kCtlBytes + (size_t)((uint64_t)world * tiles * per_tile) * sizeof(uint32_t);
+  const uint64_t ring = (uint64_t)world * ring_tiles * per_tile;
+  // two-shot: one flag per tile of each owner's share
+  const uint64_t two_shot = (uint64_t)world * std::max<uint64_t>(1, (per_owner + (uint64_t)t.chunk_bytes - 1) /
+                                                                       (uint64_t)t.chunk_bytes);
+  return (size_t)pl::kCtlBytes + (size_t)std::max(ring, two_shot) * sizeof(uint32_t);
 }
 
 purlin_status purlin_initialize(int world, void* workspace, size_t workspace_bytes, purlin_stream_t stream,

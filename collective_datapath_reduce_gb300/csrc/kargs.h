@@ -57,7 +57,10 @@ static_assert(sizeof(TraceRecord) == 32, "trace record layout");
 const void* kernel_copy(int unroll);
 const void* kernel_reduce_f32(int nsrc, int unroll);
 const void* kernel_reduce_bf16(int nsrc, int unroll);
-// Ring AllReduce (reduce items that read partial sums stored in the same launch).
+// Two-shot AllReduce with L2 priorities (store_hint 3).
+const void* kernel_reduce_l2_f32(int nsrc, int unroll);
+const void* kernel_reduce_l2_bf16(int nsrc, int unroll);
+// Ring AllReduce (reduce items that read running sums stored in the same launch).
 const void* kernel_reduce_ring_f32(int unroll);
 const void* kernel_reduce_ring_bf16(int unroll);
 // TMA bulk pipeline variants (dynamic shared memory).

@@ -246,6 +246,118 @@ __device__ void ring_stage_bf16(const char* const* src, char* const* dst, uint64
   for (uint64_t k = head + (uint64_t)nv * 8 + tid; k < n; k += nt) ring_elem_bf16<SS, SD>(src, dst, k);
 }
 
+// ------------------------------------------- L2 priorities of SNAC plans
+
+// store_hint 3 (two-shot AllReduce).  A reduce item's inputs are read once:
+// loaded with an evict-first L2 policy.  Its result (the owner's tile) is read
+// back by the copy items shortly after: stored with an evict-last policy, so
+// that the inputs streaming through the L2 do not push it out before the
+// copies read it.  The copies load it through the L2, return each line read
+// to normal priority, and store their results evict-first (.cs).  Only
+// 16-byte aligned items take these paths; any other item runs on the plain
+// Atoms.
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint4 ld_stream_policy(const void* p, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+
+__device__ __forceinline__ void st_vec_policy(void* p, uint4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w), "l"(pol)
+               : "memory");
+}
+
+__device__ __forceinline__ void l2_priority_normal(const void* p) {
+  asm volatile("applypriority.global.L2::evict_normal [%0], 128;" ::"l"(p) : "memory");
+}
+
+__device__ __forceinline__ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// N-to-1 reduce of a SNAC owner tile with L2 policies (one destination).  NS
+// sources known at compile time; falls back to the plain Atom otherwise.
+template <typename T, int NS, int U>
+__device__ __forceinline__ void reduce_owner_tile(const char* const* src, int ns, char* const* dst, uint64_t len) {
+  bool fast = NS > 0 && (len & 15u) == 0 && aligned16(dst[0]);
+  for (int s = 0; s < ns; ++s) fast = fast && aligned16(src[s]);
+  if constexpr (NS > 0) {
+    if (fast) {
+      constexpr int EPV = Elem<T>::kPerVec;
+      const uint64_t pf = l2_evict_first_policy();
+      const uint64_t ps = l2_evict_last_policy();
+      const uint32_t nv = (uint32_t)(len >> 4), step = blockDim.x;
+      uint32_t v = threadIdx.x;
+      auto body = [&](auto uu) {
+        constexpr int UU = decltype(uu)::value;
+        uint4 r[UU][NS];
+#pragma unroll
+        for (int b = 0; b < NS; ++b)
+#pragma unroll
+          for (int u = 0; u < UU; ++u) r[u][b] = ld_stream_policy(reinterpret_cast<const uint4*>(src[b]) + v + u * step, pf);
+#pragma unroll
+        for (int u = 0; u < UU; ++u) {
+          float acc[EPV];
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) acc[e] = Elem<T>::get(r[u][0], e);
+#pragma unroll
+          for (int b = 1; b < NS; ++b)
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) acc[e] = __fadd_rn(acc[e], Elem<T>::get(r[u][b], e));
+          st_vec_policy(reinterpret_cast<uint4*>(dst[0]) + v + u * step, Elem<T>::pack(acc), ps);
+        }
+      };
+      for (; v + (U - 1) * step < nv; v += U * step) body(std::integral_constant<int, U>());
+      for (; v < nv; v += step) body(std::integral_constant<int, 1>());
+      return;
+    }
+  }
+  reduce_atom<T, NS, U, false, false>(src, ns, dst, 1, len);
+}
+
+// Copy of a SNAC owner tile to the other ranks (loads through the L2, each
+// line read returned to normal priority, stores evict-first).
+__device__ __forceinline__ void copy_owner_tile(const char* src, char* const* dst, int nd, uint64_t len) {
+  bool fast = (len & 15u) == 0 && aligned16(src);
+  for (int j = 0; j < nd; ++j) fast = fast && aligned16(dst[j]);
+  if (!fast) {
+    copy_atom<true, 2, true>(src, dst, nd, len);
+    return;
+  }
+  const uint32_t nv = (uint32_t)(len >> 4), step = blockDim.x;
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  uint32_t v = threadIdx.x;
+  for (; v + step < nv; v += 2 * step) {
+    const uint4 r0 = ld_l2(s4 + v), r1 = ld_l2(s4 + v + step);
+    if ((v & 7u) == 0) l2_priority_normal(s4 + v);
+    if (((v + step) & 7u) == 0) l2_priority_normal(s4 + v + step);
+    for (int j = 0; j < nd; ++j) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst[j]);
+      st_vec<true>(d4 + v, r0);
+      st_vec<true>(d4 + v + step, r1);
+    }
+  }
+  for (; v < nv; v += step) {
+    const uint4 r = ld_l2(s4 + v);
+    if ((v & 7u) == 0) l2_priority_normal(s4 + v);
+    for (int j = 0; j < nd; ++j) st_vec<true>(reinterpret_cast<uint4*>(dst[j]) + v, r);
+  }
+}
+
 // T = void: copy-only kernel (AllGather, AllToAll and their V forms).
 // Otherwise items with one source are the consume-side copies of the
 // two-shot and ring AllReduce, whose source another CTA produced in this
@@ -290,8 +402,16 @@ __device__ __forceinline__ void run_item(const char* const* src, int ns, char* c
 template <int NS>
 constexpr int snac_max_threads() { return NS == 0 ? 256 : 512; }
 
-template <typename T, int NS, int U, bool COH = false>
+// Kernel kinds.  kKindPlain: every layout but the ring (store_hint 1 or 2).
+// kKindRing: the ring's reduce items read running sums stored in this launch.
+// kKindL2: SNAC plans with L2 priorities (store_hint 3): owner tiles reduced
+// and copied on the paths above.  Each kind is its own instantiation, so the
+// others' code never enters the plain kernel.
+enum : int { kKindPlain = 0, kKindRing = 1, kKindL2 = 2 };
+
+template <typename T, int NS, int U, int KIND = kKindPlain>
 __global__ void __launch_bounds__(snac_max_threads<NS>(), 2) snac_kernel(const __grid_constant__ KArgs a) {
+  constexpr bool COH = KIND == kKindRing;
   constexpr uint32_t kNoItem = 0xFFFFFFFFu;
   __shared__ const char* s_src[kMaxWorld];
   __shared__ char* s_dst[kMaxWorld];
@@ -369,10 +489,18 @@ __global__ void __launch_bounds__(snac_max_threads<NS>(), 2) snac_kernel(const _
     __syncthreads();
     const uint32_t i = s_item;
     if (i == kNoItem || !s_ok) break;
-    if (a.store_hint == 2)
+    if constexpr (KIND == kKindL2 && !std::is_same<T, void>::value) {
+      if (s_ns == 1)
+        copy_owner_tile(s_src[0], s_dst, s_nd, s_len);
+      else if (s_nd == 1)
+        reduce_owner_tile<T, NS, U>(s_src, s_ns, s_dst, s_len);
+      else
+        run_item<T, NS, U, false, false>(s_src, s_ns, s_dst, s_nd, s_len, s_split);
+    } else if (a.store_hint == 2) {
       run_item<T, NS, U, true, COH>(s_src, s_ns, s_dst, s_nd, s_len, s_split);
-    else
+    } else {
       run_item<T, NS, U, false, COH>(s_src, s_ns, s_dst, s_nd, s_len, s_split);
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
       if (s_notify && i + 1 != a.drop_notify) {

@@ -24,7 +24,7 @@ const void* kernel_reduce_bf16(int nsrc, int unroll) {
 // binary32 sum another CTA stored, as two 16-bit halves, earlier in this
 // launch (loads through the L2).
 const void* kernel_reduce_ring_bf16(int unroll) {
-  return unroll >= 2 ? (const void*)snac_kernel<bf16_tag, 2, 2, true> : (const void*)snac_kernel<bf16_tag, 2, 1, true>;
+  return unroll >= 2 ? (const void*)snac_kernel<bf16_tag, 2, 2, kKindRing> : (const void*)snac_kernel<bf16_tag, 2, 1, kKindRing>;
 }
 
 }  // namespace pl

@@ -23,7 +23,7 @@ const void* kernel_reduce_f32(int nsrc, int unroll) {
 // Ring AllReduce: each reduce stage adds one rank's input to the running sum
 // another CTA stored earlier in this launch (loads through the L2).
 const void* kernel_reduce_ring_f32(int unroll) {
-  return unroll >= 2 ? (const void*)snac_kernel<float, 2, 2, true> : (const void*)snac_kernel<float, 2, 1, true>;
+  return unroll >= 2 ? (const void*)snac_kernel<float, 2, 2, kKindRing> : (const void*)snac_kernel<float, 2, 1, kKindRing>;
 }
 
 }  // namespace pl

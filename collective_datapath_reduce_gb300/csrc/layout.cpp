@@ -150,6 +150,7 @@ Tune tune_table(int coll, int world, int dtype, uint64_t bytes_per_rank) {
   t.store_hint = 1;
   t.min_cta_bytes = 512;
   t.schedule = kSchedItem;
+  t.snac_lag = 2;  // two-shot: copies at least one wave of CTAs after their reduce
   switch (coll) {
     case kAllReduce:
     case kAtomReduce:
@@ -309,18 +310,22 @@ Tune tune_merge(const Tune& b, const Tune& o) {
   if (o.interleave_bytes) t.interleave_bytes = o.interleave_bytes;
   if (o.max_ctas) t.max_ctas = o.max_ctas;
   if (o.schedule) t.schedule = o.schedule;
+  if (o.snac_lag) t.snac_lag = o.snac_lag;
   return t;
 }
 
 Tune resolve_tune(int coll, int table_coll, int world, int dtype, uint64_t bytes_per_rank, const Tune& over) {
   Tune t = tune_merge(tune_table(table_coll, world, dtype, bytes_per_rank), over);
   if (coll == kAllReduce && (t.layout == kTwoShot || t.layout == kRing)) {
-    // the SNAC layouts' own best (512 threads, two CTAs per SM, write-back
-    // stores, no grid cap) unless the caller set these fields; the ring's
+    // the SNAC layouts' own best (512 threads, two CTAs per SM, no grid cap)
+    // unless the caller set these fields; the ring's
     // reduce items have two sources, so two vectors of each in flight
     if (!over.threads) t.threads = 512;
     if (!over.ctas_per_sm) t.ctas_per_sm = 2;
-    if (!over.store_hint) t.store_hint = 1;
+    // two-shot on the register path: the L2 priorities of store_hint 3 (8 x 64
+    // MiB bf16: 182 against 186 us write-back, DRAM reads 1.04 against 1.11
+    // times the algorithmic bytes)
+    if (!over.store_hint) t.store_hint = (t.layout == kTwoShot && t.path == kPathRegister) ? 3 : 1;
     if (!over.max_ctas) t.max_ctas = 0;
     if (t.layout == kRing && !over.unroll) t.unroll = 2;
     if (t.layout == kRing && !over.chunk_bytes) {
@@ -342,12 +347,13 @@ static int validate_tune(const Tune& t) {
   if (t.path != kPathRegister && t.path != kPathBulk) return PL_ERR_UNSUPPORTED;
   if (t.chunk_bytes < 1024 || t.chunk_bytes > (64 << 20) || t.chunk_bytes % 16) return PL_ERR_INVALID_ARG;
   if (t.stages < 2 || t.stages > 8) return PL_ERR_INVALID_ARG;
-  if (t.store_hint < 1 || t.store_hint > 2) return PL_ERR_INVALID_ARG;
+  if (t.store_hint < 1 || t.store_hint > 3) return PL_ERR_INVALID_ARG;
   if (t.min_cta_bytes < 16) return PL_ERR_INVALID_ARG;
   if (t.interleave_bytes < -1 || (t.interleave_bytes > 0 && (t.interleave_bytes < 512 || t.interleave_bytes % 512)))
     return PL_ERR_INVALID_ARG;
   if (t.max_ctas < 0) return PL_ERR_INVALID_ARG;
   if (t.schedule < kSchedItem || t.schedule > kSchedQueueGuided) return PL_ERR_INVALID_ARG;
+  if (t.snac_lag < 1 || t.snac_lag > 64) return PL_ERR_INVALID_ARG;
   return PL_OK;
 }
 
@@ -417,12 +423,9 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
         n_flags = (uint32_t)(world * tmax);
         uint64_t n_items = 0;
         for (int o = 0; o < world; ++o) n_items += 2 * tiles[o];
-        const uint64_t gcap = (uint64_t)p.tune.ctas_per_sm * sm_count;
+        uint64_t gcap = (uint64_t)p.tune.ctas_per_sm * sm_count;
+        if (p.tune.max_ctas > 0) gcap = std::min<uint64_t>(gcap, (uint64_t)p.tune.max_ctas);
         const uint64_t G = std::max<uint64_t>(1, std::min<uint64_t>(gcap, n_items));
-        // a copy round trails its reduce round by about two waves of CTAs, so
-        // the reduce has usually finished when its copies start (one wave:
-        // 63.8 / 193.9 us at 8 x 16 / 64 MiB; two: 53.4 / 186.0 us)
-        const uint64_t lag = std::max<uint64_t>(1, ceil_div(G, (uint64_t)world));
         auto reduce_piece = [&](int o, uint64_t t) {
           uint64_t off = start[o] + t * T, len = std::min(T, start[o + 1] - off);
           Piece q{off, off, len, ALL, 1u << o, 0, (uint32_t)(o * tmax + t + 1)};
@@ -433,13 +436,38 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
           Piece q{off, off, len, 1u << (16 + o), ALL & ~(1u << o), (uint32_t)(o * tmax + t + 1), 0};
           push_grouped(pieces, q, dst_res);
         };
-        for (uint64_t t = 0; t < tmax + lag; ++t) {
-          if (t < tmax)
-            for (int o = 0; o < world; ++o)
-              if (t < tiles[o]) reduce_piece(o, t);
-          if (t >= lag && t - lag < tmax)
-            for (int o = 0; o < world; ++o)
-              if (t - lag < tiles[o]) copy_piece(o, t - lag);
+        // Order of the items (the CTAs run item i on CTA i % G, or take them
+        // from the shared queue in this order).  Reduce and copy items
+        // alternate in a checkerboard of (wave i / G, CTA i % G): every CTA
+        // alternates the two kinds and every wave holds about as many of
+        // each.  (Rounds of world reduces then world copies gave each CTA one
+        // kind whenever G is a multiple of 2 world: at 8 x 64 MiB the reduce
+        // CTAs set the pace while the copy CTAs spent 11% of the time
+        // waiting.)  A tile's copy comes at least snac_lag x G / 2 positions
+        // after its reduce (two waves by default: the reduce has finished by
+        // then); a copy that is due but not yet allowed gives its position to
+        // the next reduce.
+        std::vector<std::pair<int, uint64_t>> tile_order;  // (owner, tile), tile-major
+        for (uint64_t t = 0; t < tmax; ++t)
+          for (int o = 0; o < world; ++o)
+            if (t < tiles[o]) tile_order.emplace_back(o, t);
+        const uint64_t nr = tile_order.size();
+        const uint64_t D = std::max<uint64_t>(1, (uint64_t)p.tune.snac_lag * G / 2);
+        std::vector<uint64_t> rpos(nr);
+        uint64_t r = 0, c = 0;
+        while (r < nr || c < nr) {
+          const uint64_t pos = pieces.size();
+          const bool want_r = (((pos / G) + (pos % G)) & 1u) == 0;
+          const bool can_r = r < nr, can_c = c < r && rpos[c] + D <= pos;
+          const bool do_r = can_r && (want_r || !can_c);
+          if (do_r) {
+            rpos[r] = pos;
+            reduce_piece(tile_order[r].first, tile_order[r].second);
+            ++r;
+          } else {
+            copy_piece(tile_order[c].first, tile_order[c].second);
+            ++c;
+          }
         }
       } else if (p.tune.layout == kRing && world > 1) {
         // Ring (Iris docs, "Device Context", all_reduce_ring: a running sum
@@ -522,6 +550,9 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
               if (t < tiles[j]) stage_piece(j, t, st);
           }
       } else {
+        // one rank: every layout is the one-shot copy (and the two-shot's L2
+        // priorities have no copies to serve)
+        if (p.tune.layout == kTwoShot && p.tune.store_hint == 3) p.tune.store_hint = 1;
         p.tune.layout = kOneShot;
         push_grouped(pieces, Piece{0, 0, S, ALL, ALL, 0, 0}, dst_res);
       }
@@ -641,6 +672,11 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
       break;
     }
   }
+  // store_hint 3 keeps reduce results evict-last in the L2 until a copy has
+  // read them back: only the two-shot layout (register path) has such copies
+  if (p.tune.store_hint == 3 &&
+      !(coll == kAllReduce && p.tune.layout == kTwoShot && sync && p.tune.path == kPathRegister))
+    return PL_ERR_INVALID_ARG;
   if (!p.reduce) p.nsrc = 1;
   // the register-path kernel for more than 8 sources is built for CTAs of at
   // most 256 threads (room for 128 registers)
@@ -831,13 +867,50 @@ std::string check_plan(const Plan& p) {
     if (it.wait) {
       if (it.wait > (uint32_t)p.n_flags) return "wait flag out of range";
       const int64_t at = notified_at[it.wait - 1];
-      if (at < 0 || at >= (int64_t)i) return "wait without an earlier notify";
+      if (at < 0) return "wait without a notify";
+      // strided and queued plans: every wait follows its notify in the
+      // global order (the queue hands items out in that order)
+      if ((p.strided || p.queue) && at >= (int64_t)i) return "wait without an earlier notify";
     }
+  }
+  if (p.sync && !p.queue) {
+    // the CTAs' sequences and the waits must not form a cycle (all CTAs are
+    // resident, so then the earliest unfinished item can always run)
+    const size_t n = p.items.size();
+    std::vector<std::vector<uint32_t>> out(n);
+    std::vector<uint32_t> indeg(n, 0);
+    auto edge = [&](size_t a, size_t b) {
+      out[a].push_back((uint32_t)b);
+      ++indeg[b];
+    };
+    if (p.strided) {
+      for (size_t i = 0; i + (size_t)p.grid < n; ++i) edge(i, i + (size_t)p.grid);
+    } else {
+      if (p.cta_begin.size() != (size_t)p.grid + 1 || p.cta_begin.front() != 0 || p.cta_begin.back() != n)
+        return "cta ranges";
+      for (size_t c = 0; c + 1 < p.cta_begin.size(); ++c)
+        for (uint32_t i = p.cta_begin[c]; i + 1 < p.cta_begin[c + 1]; ++i) edge(i, i + 1);
+    }
+    for (size_t i = 0; i < n; ++i)
+      if (p.items[i].wait) edge((size_t)notified_at[p.items[i].wait - 1], i);
+    std::vector<uint32_t> ready;
+    for (size_t i = 0; i < n; ++i)
+      if (!indeg[i]) ready.push_back((uint32_t)i);
+    size_t done = 0;
+    while (!ready.empty()) {
+      const uint32_t i = ready.back();
+      ready.pop_back();
+      ++done;
+      for (uint32_t j : out[i])
+        if (--indeg[j] == 0) ready.push_back(j);
+    }
+    if (done != n) return "the waits of the plan can deadlock";
   }
   // item b comes after item a through a chain of waits: b waits for a flag
   // that a, or an item after a in that sense, notified
-  auto chained = [&](int64_t a, int64_t b) {
-    for (int64_t k = b; k > a;) {
+  auto chain_to = [&](int64_t a, int64_t b) {
+    int64_t k = b;
+    for (size_t hops = 0; hops <= p.items.size(); ++hops) {
       const uint32_t w = p.items[(size_t)k].wait;
       if (!w) return false;
       k = notified_at[w - 1];
@@ -845,6 +918,7 @@ std::string check_plan(const Plan& p) {
     }
     return false;
   };
+  auto chained = [&](int64_t a, int64_t b) { return chain_to(a, b) || chain_to(b, a); };
   for (int r = 0; r < p.world; ++r) {
     auto& v = acc[r];
     std::sort(v.begin(), v.end(), [](const Acc& x, const Acc& y) {

@@ -46,8 +46,9 @@ struct NaArgs {
   uint32_t elem;             // bytes per element
   uint32_t world;
   uint32_t tmax;             // tiles of the largest owner range
-  uint32_t lag;              // rounds between a tile's reduce and its copies
-  uint32_t slots;            // (tmax + lag) rounds of 2 * world slots
+  uint32_t half;             // reduce slots (and copy slots) per wave: grid / 2
+  uint32_t lag;              // copy slots before the first copy: one wave
+  uint32_t slots;            // waves x grid
   uint32_t dst_coaligned;    // every output has the same address residue mod 16
   uint32_t drop_notify;      // test hook: 1 + flag whose notify is skipped, or 0
 };
@@ -80,18 +81,32 @@ __global__ void __launch_bounds__(kNaThreads, 2) noalloc_kernel(const __grid_con
   __shared__ uint32_t s_flag, s_epoch;
 
   const uint32_t N = a.world;
+  const uint32_t G = gridDim.x, c = blockIdx.x;
   if (threadIdx.x == 0) s_epoch = ld_volatile(a.scratch + kNaEpoch) + 1u;
-  for (uint32_t slot = blockIdx.x; slot < a.slots; slot += gridDim.x) {
+  // Slot s runs on CTA s % G in increasing order.  Reduce and copy slots
+  // alternate in a checkerboard of (wave s / G, CTA): every CTA alternates
+  // the two kinds, and each wave holds `half` of each.  Reduce slot k takes
+  // tile k (tile-major over the owners); copy slot k takes tile k - lag, one
+  // wave after its reduce, so every wait points to an earlier slot.
+  for (uint32_t slot = c; slot < a.slots; slot += G) {
     if (threadIdx.x == 0) {
-      const uint32_t round = slot / (2 * N), k = slot % (2 * N);
-      const bool reduce = k < N;
-      const uint32_t o = reduce ? k : k - N;
-      const int64_t t = reduce ? (int64_t)round : (int64_t)round - (int64_t)a.lag;
+      const uint32_t w = slot / G;
+      const bool reduce = ((w + c) & 1u) == 0;
+      const uint32_t before = (reduce == ((w & 1u) == 0)) ? (c + 1) / 2 : c / 2;
+      const int64_t idx = (int64_t)w * a.half + before - (reduce ? 0 : (int64_t)a.lag);
+      const uint64_t nt = (uint64_t)a.tmax * N;
+      int kind = 0;
+      uint32_t o = 0;
+      int64_t t = -1;
+      if (idx >= 0 && (uint64_t)idx < nt) {
+        t = idx / N;
+        o = (uint32_t)(idx % N);
+        kind = reduce ? 1 : 2;
+      }
       const uint64_t olen = (a.q + (o < a.rem ? 1 : 0)) * a.elem;
       const uint64_t ostart = ((uint64_t)o * a.q + (o < a.rem ? o : a.rem)) * a.elem;
-      int kind = 0;
-      if (t >= 0 && (uint64_t)t * kNaTile < olen) kind = reduce ? 1 : 2;
-      if (kind && N == 1 && kind == 2) kind = 0;
+      if (kind && (uint64_t)t * kNaTile >= olen) kind = 0;
+      if (kind == 2 && N == 1) kind = 0;
       int ok = 1;
       if (kind) {
         const uint64_t off = ostart + (uint64_t)t * kNaTile;
@@ -119,16 +134,19 @@ __global__ void __launch_bounds__(kNaThreads, 2) noalloc_kernel(const __grid_con
     }
     __syncthreads();
     if (!s_ok) break;
+    // owner tiles with the L2 policies of the library's two-shot plans
+    // (inputs evict-first, the owner tile evict-last until its copy has read
+    // it, copies evict-first)
     if (s_kind == 1) {
       if (s_ns == 1)
         copy_atom<false, 2, false>(s_src[0], s_dst, 1, s_len);
       else
-        reduce_atom<T, NS, 1, false>(s_src, s_ns, s_dst, 1, s_len);
+        reduce_owner_tile<T, NS, 1>(s_src, s_ns, s_dst, s_len);
     } else if (s_kind == 2) {
       if (a.dst_coaligned) {
-        copy_atom<true, 2, false>(s_src[0], s_dst, s_nd, s_len);
+        copy_owner_tile(s_src[0], s_dst, s_nd, s_len);
       } else {
-        for (int j = 0; j < s_nd; ++j) copy_atom<true, 2, false>(s_src[0], s_dst + j, 1, s_len);
+        for (int j = 0; j < s_nd; ++j) copy_atom<true, 2, true>(s_src[0], s_dst + j, 1, s_len);
       }
     }
     __syncthreads();
@@ -303,7 +321,7 @@ extern "C" purlin_status purlin_all_reduce_noalloc(int world, const void* const*
     a.out[r] = (char*)dst[r];
     if ((((uintptr_t)dst[r]) & 15u) != (((uintptr_t)dst[0]) & 15u)) same = 0;
   }
-  const int ctas = std::min(occ, 2) * d.sm_count;
+  int ctas = std::min(occ, 2) * d.sm_count;
   a.scratch = d.scratch;
   a.device_status = device_status;
   a.timeout_ns = 2000000000ull;
@@ -319,12 +337,15 @@ extern "C" purlin_status purlin_all_reduce_noalloc(int world, const void* const*
   a.elem = (uint32_t)E;
   a.world = (uint32_t)world;
   a.tmax = (uint32_t)tmax;
-  // copies trail their reduce by about two waves of CTAs (as the library's
-  // two-shot plans): the reduce has usually finished when its copies start
-  a.lag = (uint32_t)std::max<uint64_t>(1, ((uint64_t)ctas + world - 1) / (uint64_t)world);
-  a.slots = (uint32_t)((tmax + a.lag) * 2ull * (uint64_t)world);
+  // an even grid (the checkerboard of slots), no larger than two slots per tile
+  const uint64_t nt = tmax * (uint64_t)world;
+  uint64_t g = std::min<uint64_t>((uint64_t)ctas, 2 * nt);
+  g = std::max<uint64_t>(2, g & ~1ull);
+  a.half = (uint32_t)(g / 2);
+  a.lag = a.half;  // copies one wave after their reduce
+  a.slots = (uint32_t)(((nt + a.lag + a.half - 1) / a.half) * g);
   a.dst_coaligned = same;
-  const int grid = (int)std::min<uint64_t>((uint64_t)ctas, a.slots);
+  const int grid = (int)g;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);

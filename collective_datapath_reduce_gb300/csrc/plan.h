@@ -84,6 +84,7 @@ struct Tune {
   int interleave_bytes = 0;  // > 0: parts of about this size, CTA c takes parts c, c + grid, ...
   int max_ctas = 0;          // > 0: cap on the grid size
   int schedule = 0;          // Schedule
+  int snac_lag = 0;          // two-shot: positions between a tile's reduce and its copies, in half waves
 };
 
 struct Plan {

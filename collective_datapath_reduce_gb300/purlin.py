@@ -57,7 +57,7 @@ class PurlinError(RuntimeError):
 class purlin_tune(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "layout", "ctas_per_sm", "threads", "unroll", "path", "chunk_bytes", "stages",
-        "store_hint", "min_cta_bytes", "interleave_bytes", "max_ctas", "schedule")]
+        "store_hint", "min_cta_bytes", "interleave_bytes", "max_ctas", "schedule", "snac_lag")]
 
 
 class purlin_item(ctypes.Structure):

@@ -133,13 +133,20 @@ typedef struct {
                        layouts (ring default: a 64th of bytes_per_rank / world, kept
                        between 64 and 128 KiB) */
   int stages;       /* TMA pipeline depth, 2..8 */
-  int store_hint;   /* 1 = default write-back stores, 2 = streaming (evict-first) stores */
+  int store_hint;   /* register path: 1 = write-back stores, 2 = streaming (evict-first)
+                       stores; 3 = L2 priorities of the two-shot AllReduce (only there,
+                       else PL_ERR_INVALID_ARG): reduce inputs loaded evict-first, owner
+                       tiles stored evict-last until their copies have read them, copies
+                       stored evict-first */
   int min_cta_bytes;/* fewest work bytes given to one CTA before the grid shrinks */
   int interleave_bytes; /* a multiple of 512: the work is cut into k x grid parts of about
                            this size and CTA c takes parts c, c + grid, ...; -1: one
                            contiguous share per CTA (0 = the table's choice) */
   int max_ctas;     /* > 0: at most this many CTAs (fewer concurrent DRAM streams) */
   int schedule;     /* purlin_schedule: how CTAs walk their items */
+  int snac_lag;     /* two-shot AllReduce: a tile's copies come at least snac_lag x grid / 2
+                       places after its reduce in the items' order (1..64; table: 4, two
+                       waves of CTAs) */
 } purlin_tune;
 
 /* How the CTAs of a launch walk the plan's work items (purlin_tune.schedule).

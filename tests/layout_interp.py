@@ -18,9 +18,44 @@ import oracle
 SPLIT_SRC, SPLIT_DST = 1 << 30, 1 << 31
 
 
-def run_items(items, ins, outs, dtype):
-    """ins / outs: lists of uint8 arrays (rank buffers as bytes)."""
-    for it in items:
+QUEUED = 0xFFFFFFFF
+
+
+def schedule(items):
+    """The items in an order a grid of CTAs could run them: each CTA's items
+    in its own order ("order" field), an item that waits only after the item
+    that notifies its flag.  CTAs are stepped round-robin, each running
+    whatever it can; a pass with no progress means the plan deadlocks.
+    Queued items (any CTA) run in their global order."""
+    if not items or "cta" not in items[0] or all(it["cta"] == QUEUED for it in items):
+        return list(items)
+    by_cta = {}
+    for i, it in enumerate(items):
+        by_cta.setdefault(it["cta"], []).append((it["order"], i))
+    seqs = {c: [i for _, i in sorted(v)] for c, v in by_cta.items()}
+    head = {c: 0 for c in seqs}
+    flags, out = set(), []
+    while len(out) < len(items):
+        progress = False
+        for c, seq in seqs.items():
+            while head[c] < len(seq):
+                it = items[seq[head[c]]]
+                if it["wait"] and it["wait"] not in flags:
+                    break
+                out.append(it)
+                if it["notify"]:
+                    flags.add(it["notify"])
+                head[c] += 1
+                progress = True
+        assert progress, "the plan's waits deadlock"
+    return out
+
+
+def run_items(items, ins, outs, dtype, as_given=False):
+    """ins / outs: lists of uint8 arrays (rank buffers as bytes).  Items are
+    applied in an order the CTAs could run them (schedule()), or as given
+    (as_given: the caller orders them)."""
+    for it in (items if as_given else schedule(items)):
         n = int(it["len"])
         so, do = int(it["src_off"]), int(it["dst_off"])
         srcs = []

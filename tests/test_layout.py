@@ -78,15 +78,43 @@ def test_all_reduce_plan(world, dtype, layout):
                 assert np.array_equal(outs[r], _bytes(want[r])), (n, sm, r)
             if layout == P.PL_LAYOUT_TWO_SHOT and world > 1:
                 assert nflags > 0
-                first_notify = {}
+                notify_at, kinds = {}, {}
                 for i, it in enumerate(items):
                     if it["notify"]:
-                        first_notify[it["notify"]] = i
-                for i, it in enumerate(items):
+                        notify_at[it["notify"]] = i
                     if it["wait"]:
-                        assert first_notify[it["wait"]] < i
-                        # strided: a CTA runs its items in increasing global order
-                        assert it["cta"] == i % grid
+                        # every copy follows its reduce; a CTA runs its items in
+                        # increasing global order (item i on CTA i % grid)
+                        assert notify_at[it["wait"]] < i
+                    assert it["cta"] == i % grid
+                    kinds.setdefault(it["cta"], set()).add(popcount(it["src_mask"]) > 1)
+                if len(items) >= 4 * grid and len(set(dres)) == 1:
+                    # reduces and copies alternate on every CTA (none runs only
+                    # one kind; copies split by destination alignment shift it)
+                    assert all(k == {True, False} for k in kinds.values())
+
+
+@pytest.mark.parametrize("world", [2, 3, 8])
+def test_two_shot_queue_order(world):
+    """Two-shot on the shared queue: items in one global order in which every
+    copy follows its reduce."""
+    E = 2
+    for n in (1000, 4096 + 3, 300007):
+        ins = [_draw("bf16", n) for _ in range(world)]
+        tune = {"layout": P.PL_LAYOUT_TWO_SHOT, "chunk_bytes": 1024, "schedule": P.PL_SCHED_QUEUE}
+        items, grid, nflags = _describe(P.PL_COLL_ALL_REDUCE, world, P.PL_BF16, [n * E], sm=7, tune=tune)
+        assert all(it["cta"] == QUEUED for it in items)
+        outs = [np.zeros(n * E, np.uint8) for _ in range(world)]
+        run_items(items, [_bytes(x) for x in ins], outs, "bf16")
+        want = oracle.all_reduce(ins, "bf16")
+        for r in range(world):
+            assert np.array_equal(outs[r], _bytes(want[r])), (n, r)
+        at = {}
+        for i, it in enumerate(items):
+            if it["notify"]:
+                at[it["notify"]] = i
+            if it["wait"]:
+                assert at[it["wait"]] < i
 
 
 SPLIT_SRC, SPLIT_DST = 1 << 30, 1 << 31
@@ -455,7 +483,7 @@ def test_default_workspace_holds_the_snac_layouts_flags():
     it; purlin_workspace_bytes sizes a workspace for a larger maximum."""
     default = _header_define("PURLIN_DEFAULT_WORKSPACE_FLAGS")
     GiB = 1 << 30
-    for world, S in ((8, 9 * GiB), (16, 4 * GiB), (2, 64 * GiB), (8, 64 << 20)):
+    for world, S in ((8, 9 * GiB), (16, 4 * GiB), (2, 32 * GiB), (8, 64 << 20), (3, 1000)):
         for layout in (P.PL_LAYOUT_TWO_SHOT, P.PL_LAYOUT_RING):
             st, _, _, nflags = P.purlin_plan_describe(P.PL_COLL_ALL_REDUCE, world, P.PL_BF16, [S], None, None, 152,
                                                       {"layout": layout}, items=False)

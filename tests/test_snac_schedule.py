@@ -38,7 +38,7 @@ def run_threads(items, grid, ins, outs, dtype, drop=None, timeout=5.0):
                         status["failed"] = True
                         cond.notify_all()
                         return
-            run_items([it], ins, outs, dtype)   # the item's data movement
+            run_items([it], ins, outs, dtype, as_given=True)   # the item's data movement
             if it["notify"] and i != drop:
                 with cond:
                     flags[it["notify"]] = True
