@@ -266,7 +266,8 @@ def recorded_traffic(name, tune):
 
 def run_own(args, dist):
     import torch
-    from collective_datapath_reduce_gb300 import _build, inputs
+    import workload_inputs as inputs
+from collective_datapath_reduce_gb300 import _build
     from collective_datapath_reduce_gb300 import purlin as P
 
     _build.build()
@@ -607,7 +608,7 @@ def side_table(P, h, stream, dev):
         del x, y, one_shot
     torch.cuda.empty_cache()
     # ReduceScatterV: uneven chunks (workload 5's first row of counts), bf16
-    from collective_datapath_reduce_gb300 import inputs as _inputs
+    import workload_inputs as _inputs
     C5, _ = _inputs.w5_counts(WORLD)
     counts = [int(v) * 2 for v in C5[0]]
     total = sum(counts)
@@ -720,7 +721,7 @@ def host_cpu():
 def _reference_call(name):
     """The oracle function of a workload: f(list of rank arrays) -> outputs."""
     import oracle
-    from collective_datapath_reduce_gb300 import inputs
+    import workload_inputs as inputs
     C5, c5 = inputs.w5_counts(WORLD)
     return {
         "allreduce_bf16_8x64MiB": lambda ins: oracle.all_reduce(ins, "bf16"),
@@ -793,7 +794,7 @@ def run_reference(args, dist):
     full); rank 0 only."""
     if dist.rank != 0:
         return
-    from collective_datapath_reduce_gb300 import inputs
+    import workload_inputs as inputs
     from collective_datapath_reduce_gb300 import purlin as P  # names only: the library is not loaded
     wl = workloads(P, inputs)[args.workload]
     x = [np.asarray(a) for a in wl.make_inputs()]

@@ -101,7 +101,7 @@ def pin_dim0_definitions(oracle):
 
 def pin_integer_exact(oracle, world=2, n=1024, seed=0):
     """Integer data: every order of additions gives the exact sum."""
-    from collective_datapath_reduce_gb300 import inputs
+    import workload_inputs as inputs
     x = inputs.w1_allreduce_ints(world, n, seed)
     exact = x.astype(np.int64).sum(axis=0)
     for dtype in ("f32", "bf16"):

@@ -61,7 +61,7 @@ def test_both_arms_describe_the_workload_alike():
     the workload alone, so the two lines of a workload carry equal objects."""
     sys.path.insert(0, ROOT)
     import bench
-    from collective_datapath_reduce_gb300 import inputs
+    import workload_inputs as inputs
     from collective_datapath_reduce_gb300 import purlin as P
     wl = bench.workloads(P, inputs)[WORKLOAD]
     x = wl.make_inputs()

@@ -13,7 +13,7 @@ import torch
 
 import oracle
 from collective_datapath_reduce_gb300 import examples as EX
-from collective_datapath_reduce_gb300 import inputs
+import workload_inputs as inputs
 
 pytestmark = pytest.mark.gpu
 

@@ -17,7 +17,8 @@ import pytest
 import torch
 
 import oracle
-from collective_datapath_reduce_gb300 import _build, inputs
+import workload_inputs as inputs
+from collective_datapath_reduce_gb300 import _build
 from collective_datapath_reduce_gb300 import purlin as P
 from gpu_util import Handle, RankBuffers, stream, sync
 

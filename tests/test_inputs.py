@@ -2,7 +2,7 @@
 
 import numpy as np
 
-from collective_datapath_reduce_gb300 import inputs
+import workload_inputs as inputs
 
 
 def test_generators_are_seeded():

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from collective_datapath_reduce_gb300 import inputs
+import workload_inputs as inputs
 from collective_datapath_reduce_gb300 import torch_api as purlin
 
 
