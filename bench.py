@@ -267,7 +267,7 @@ def recorded_traffic(name, tune):
 def run_own(args, dist):
     import torch
     import workload_inputs as inputs
-from collective_datapath_reduce_gb300 import _build
+    from collective_datapath_reduce_gb300 import _build
     from collective_datapath_reduce_gb300 import purlin as P
 
     _build.build()

@@ -29,7 +29,7 @@ import torch
 import oracle
 from collective_datapath_reduce_gb300 import _build
 from collective_datapath_reduce_gb300 import purlin as P
-from collective_datapath_reduce_gb300.inputs import Tiled
+from workload_inputs import Tiled
 from gpu_util import Handle, RankBuffers, stream, sync
 
 pytestmark = pytest.mark.gpu
