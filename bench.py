@@ -542,7 +542,7 @@ def side_table(P, h, stream, dev):
             d["l2_resident"] = True
         return d
 
-    out = {"d2d_copy": {}, "all_gather_u8": {}, "all_to_all_u8": {}, "all_reduce_bf16": {},
+    out = {"d2d_copy": {}, "launch_floor": {}, "all_gather_u8": {}, "all_to_all_u8": {}, "all_reduce_bf16": {},
            "reduce_scatter_f32": {}, "all_reduce_two_shot_bf16": {}, "all_reduce_ring_bf16": {},
            "reduce_scatter_v_bf16": {},
            "device_api_fused": {}, "atom_copy": {}, "atom_reduce": {}}
@@ -565,6 +565,9 @@ def side_table(P, h, stream, dev):
         out["d2d_copy"][key] = point(2 * half, timeit(lambda: big[half:].copy_(big[:half]), graph=False))
         del src, da, big
         torch.cuda.empty_cache()
+    # the floor of a call in a CUDA graph of 10: torch's one-element fill kernel
+    tiny = torch.zeros(1, dtype=torch.float32, device=dev)
+    out["launch_floor"] = {"torch_fill_1_element": point(4, timeit(lambda: tiny.fill_(1.0)))}
     for size in (64 << 10, 1 * MI, 16 * MI, 64 * MI, 256 * MI):
         key = f"{size >> 10}KiB" if size < MI else f"{size >> 20}MiB"
         x = bufs(size // 2, WORLD, torch.bfloat16)
