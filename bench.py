@@ -543,7 +543,8 @@ def side_table(P, h, stream, dev):
         return d
 
     out = {"d2d_copy": {}, "launch_floor": {}, "all_gather_u8": {}, "all_to_all_u8": {}, "all_reduce_bf16": {},
-           "reduce_scatter_f32": {}, "all_reduce_two_shot_bf16": {}, "all_reduce_ring_bf16": {},
+           "reduce_scatter_f32": {}, "all_reduce_two_shot_bf16": {}, "all_reduce_two_shot_fused_bf16": {},
+           "all_reduce_ring_bf16": {},
            "reduce_scatter_v_bf16": {},
            "device_api_fused": {}, "atom_copy": {}, "atom_reduce": {}}
     chk = lambda st: P.check(st)
@@ -577,6 +578,7 @@ def side_table(P, h, stream, dev):
         if size >= 16 * MI:
             one_shot = [t.clone() for t in y]
             for layout, name in ((P.PL_LAYOUT_TWO_SHOT, "all_reduce_two_shot_bf16"),
+                                 (P.PL_LAYOUT_TWO_SHOT_FUSED, "all_reduce_two_shot_fused_bf16"),
                                  (P.PL_LAYOUT_RING, "all_reduce_ring_bf16")):
                 P.check(P.purlin_tune_override(h, {"layout": layout}))
                 for t in y:

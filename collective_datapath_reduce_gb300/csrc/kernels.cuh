@@ -100,6 +100,14 @@ __device__ __forceinline__ bool item_in_bounds(const KArgs& a, const Item& it) {
 #ifdef PURLIN_DEBUG
   const uint64_t end = it.src_off + it.len;
   if (end < it.src_off || it.dst_off + it.len < it.dst_off) return false;
+  if (it.dst_mask & kFused) {  // inputs and the reduced destination at src_off, the copy at dst_off
+    for (uint32_t m = it.src_mask & 0xFFFFu; m; m &= m - 1)
+      if (end > a.in_bytes[__ffs(m) - 1]) return false;
+    if (end > a.out_bytes[__ffs(it.dst_mask & kDstRanks) - 1]) return false;
+    for (int d = 0; d < a.nsrc; ++d)
+      if (it.dst_off + it.len > a.out_bytes[d]) return false;
+    return true;
+  }
   for (uint32_t m = it.src_mask; m; m &= m - 1) {
     const int b = __ffs(m) - 1;
     if (end > (b < 16 ? a.in_bytes[b] : a.out_bytes[b - 16])) return false;
@@ -358,6 +366,47 @@ __device__ __forceinline__ void copy_owner_tile(const char* src, char* const* ds
   }
 }
 
+// A fused two-shot item (kFused): reduce the owner tile whose NS sources are
+// src[] into dst[0], and in the same pass copy the tile at src_b (another
+// CTA's owner tile, reduced earlier in this launch) to dst[1 .. nb]: per
+// vector NS + 1 loads and 1 + nb stores, the one-shot layout's mix.  Falls
+// back to the two parts one after the other when a pointer is not 16-byte
+// aligned or the source count is not known at compile time.
+template <typename T, int NS, int U>
+__device__ __forceinline__ void fused_owner_tiles(const char* const* src, int ns, char* const* dst, const char* src_b,
+                                                  int nb, uint64_t len) {
+  if constexpr (NS > 0) {
+    bool fast = (len & 15u) == 0 && aligned16(dst[0]) && aligned16(src_b);
+    for (int s = 0; s < NS; ++s) fast = fast && aligned16(src[s]);
+    for (int j = 1; j <= nb; ++j) fast = fast && aligned16(dst[j]);
+    if (fast) {
+      constexpr int EPV = Elem<T>::kPerVec;
+      const uint64_t pf = l2_evict_first_policy(), pl = l2_evict_last_policy();
+      const uint32_t nv = (uint32_t)(len >> 4), step = blockDim.x;
+      const uint4* sb = reinterpret_cast<const uint4*>(src_b);
+      for (uint32_t v = threadIdx.x; v < nv; v += step) {
+        uint4 r[NS];
+#pragma unroll
+        for (int b = 0; b < NS; ++b) r[b] = ld_stream_policy(reinterpret_cast<const uint4*>(src[b]) + v, pf);
+        const uint4 y = ld_l2(sb + v);
+        if ((v & 7u) == 0) l2_priority_normal(sb + v);
+        float acc[EPV];
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) acc[e] = Elem<T>::get(r[0], e);
+#pragma unroll
+        for (int b = 1; b < NS; ++b)
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) acc[e] = __fadd_rn(acc[e], Elem<T>::get(r[b], e));
+        st_vec_policy(reinterpret_cast<uint4*>(dst[0]) + v, Elem<T>::pack(acc), pl);
+        for (int j = 1; j <= nb; ++j) st_vec<true>(reinterpret_cast<uint4*>(dst[j]) + v, y);
+      }
+      return;
+    }
+  }
+  reduce_owner_tile<T, NS, U>(src, ns, dst, len);
+  copy_owner_tile(src_b, dst + 1, nb, len);
+}
+
 // T = void: copy-only kernel (AllGather, AllToAll and their V forms).
 // Otherwise items with one source are the consume-side copies of the
 // two-shot and ring AllReduce, whose source another CTA produced in this
@@ -418,6 +467,7 @@ __global__ void __launch_bounds__(snac_max_threads<NS>(), 2) snac_kernel(const _
   __shared__ uint64_t s_len;
   __shared__ int s_ns, s_nd, s_ok;
   __shared__ uint32_t s_item, s_notify, s_epoch, s_wait_ns, s_split;
+  __shared__ const char* s_fsrc;  // fused items: the copied tile
   __shared__ uint32_t s_next_i, s_q_i;  // thread 0's item cursor (kept out of the registers of the Atoms)
   __shared__ unsigned long long s_t0;
   grid_dep_wait();
@@ -463,14 +513,25 @@ __global__ void __launch_bounds__(snac_max_threads<NS>(), 2) snac_kernel(const _
         }
         s_item = i;
         int ns = 0, nd = 0;
-        for (uint32_t m = it.src_mask; m; m &= m - 1) {
-          const int b = __ffs(m) - 1;
-          s_src[ns++] = (b < 16 ? a.in[b] : a.out[b - 16]) + it.src_off;
+        if (KIND == kKindL2 && (it.dst_mask & kFused)) {
+          // reduce the tile at src_off into the one destination bit; copy the
+          // tile at dst_off from the output source bit to every other output
+          for (uint32_t m = it.src_mask & 0xFFFFu; m; m &= m - 1) s_src[ns++] = a.in[__ffs(m) - 1] + it.src_off;
+          const int ob = __ffs(it.src_mask >> 16) - 1;
+          s_fsrc = a.out[ob] + it.dst_off;
+          s_dst[nd++] = a.out[__ffs(it.dst_mask & kDstRanks) - 1] + it.src_off;
+          for (int d = 0; d < a.nsrc; ++d)
+            if (d != ob) s_dst[nd++] = a.out[d] + it.dst_off;
+        } else {
+          for (uint32_t m = it.src_mask; m; m &= m - 1) {
+            const int b = __ffs(m) - 1;
+            s_src[ns++] = (b < 16 ? a.in[b] : a.out[b - 16]) + it.src_off;
+          }
+          for (uint32_t m = it.dst_mask & kDstRanks; m; m &= m - 1) s_dst[nd++] = a.out[__ffs(m) - 1] + it.dst_off;
         }
-        for (uint32_t m = it.dst_mask & kDstRanks; m; m &= m - 1) s_dst[nd++] = a.out[__ffs(m) - 1] + it.dst_off;
         s_ns = ns;
         s_nd = nd;
-        s_split = it.dst_mask & (kSplitSrc | kSplitDst);
+        s_split = it.dst_mask & (kSplitSrc | kSplitDst | kFused);
         s_len = it.len;
         if (!item_in_bounds(a, it)) {  // checking build: move nothing, keep the SNAC order
           atomicCAS(&a.ctl[kCtlStatus], 0u, (uint32_t)kDevBounds);
@@ -490,7 +551,9 @@ __global__ void __launch_bounds__(snac_max_threads<NS>(), 2) snac_kernel(const _
     const uint32_t i = s_item;
     if (i == kNoItem || !s_ok) break;
     if constexpr (KIND == kKindL2 && !std::is_same<T, void>::value) {
-      if (s_ns == 1)
+      if (s_split & kFused)
+        fused_owner_tiles<T, NS, U>(s_src, s_ns, s_dst, s_fsrc, s_nd - 1, s_len);
+      else if (s_ns == 1)
         copy_owner_tile(s_src[0], s_dst, s_nd, s_len);
       else if (s_nd == 1)
         reduce_owner_tile<T, NS, U>(s_src, s_ns, s_dst, s_len);

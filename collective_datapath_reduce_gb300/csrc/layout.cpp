@@ -316,7 +316,7 @@ Tune tune_merge(const Tune& b, const Tune& o) {
 
 Tune resolve_tune(int coll, int table_coll, int world, int dtype, uint64_t bytes_per_rank, const Tune& over) {
   Tune t = tune_merge(tune_table(table_coll, world, dtype, bytes_per_rank), over);
-  if (coll == kAllReduce && (t.layout == kTwoShot || t.layout == kRing)) {
+  if (coll == kAllReduce && (t.layout == kTwoShot || t.layout == kTwoShotFused || t.layout == kRing)) {
     // the SNAC layouts' own best (512 threads, two CTAs per SM, no grid cap)
     // unless the caller set these fields; the ring's
     // reduce items have two sources, so two vectors of each in flight
@@ -325,7 +325,8 @@ Tune resolve_tune(int coll, int table_coll, int world, int dtype, uint64_t bytes
     // two-shot on the register path: the L2 priorities of store_hint 3 (8 x 64
     // MiB bf16: 182 against 186 us write-back, DRAM reads 1.04 against 1.11
     // times the algorithmic bytes)
-    if (!over.store_hint) t.store_hint = (t.layout == kTwoShot && t.path == kPathRegister) ? 3 : 1;
+    if (!over.store_hint)
+      t.store_hint = ((t.layout == kTwoShot || t.layout == kTwoShotFused) && t.path == kPathRegister) ? 3 : 1;
     if (!over.max_ctas) t.max_ctas = 0;
     if (t.layout == kRing && !over.unroll) t.unroll = 2;
     if (t.layout == kRing && !over.chunk_bytes) {
@@ -340,7 +341,7 @@ Tune resolve_tune(int coll, int table_coll, int world, int dtype, uint64_t bytes
 }
 
 static int validate_tune(const Tune& t) {
-  if (t.layout < kOneShot || t.layout > kRing) return PL_ERR_UNSUPPORTED;
+  if (t.layout < kOneShot || t.layout > kTwoShotFused) return PL_ERR_UNSUPPORTED;
   if (t.threads < 64 || t.threads > 512 || t.threads % 32) return PL_ERR_INVALID_ARG;
   if (t.ctas_per_sm < 1 || t.ctas_per_sm > 32) return PL_ERR_INVALID_ARG;
   if (t.unroll < 1 || t.unroll > 8) return PL_ERR_INVALID_ARG;
@@ -407,7 +408,7 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
       p.work_bytes = 2ull * world * S;
       p.reduce = true;
       p.nsrc = world;
-      if (p.tune.layout == kTwoShot && world > 1) {
+      if ((p.tune.layout == kTwoShot || p.tune.layout == kTwoShotFused) && world > 1) {
         sync = true;
         const uint64_t n = S / E;
         const uint64_t T = std::max<uint64_t>(16, (uint64_t)p.tune.chunk_bytes / 16 * 16);
@@ -455,6 +456,49 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
         const uint64_t D = std::max<uint64_t>(1, (uint64_t)p.tune.snac_lag * G / 2);
         std::vector<uint64_t> rpos(nr);
         uint64_t r = 0, c = 0;
+        if (p.tune.layout == kTwoShotFused) {
+          if (p.tune.store_hint != 3 || p.tune.schedule != kSchedItem || p.tune.path != kPathRegister)
+            return PL_ERR_UNSUPPORTED;  // the L2 kernel kind runs fused items, one CTA sequence each
+          // Fused order (the L2 kernel kind): after a first wave of reduces,
+          // each item reduces the next tile and, in the same pass, copies the
+          // tile reduced D + 1 places earlier -- by the next CTA back, one
+          // wave ago (its flag is the item's wait).  Every CTA then streams 8
+          // reads and 8 writes per vector, the mix of the one-shot layout,
+          // while the copies still consume what other CTAs produced.  Tiles
+          // of unequal length (an owner's last), or whose copy destinations
+          // sit at different addresses modulo 16, go as separate items.
+          auto tile = [&](uint64_t k, uint64_t& off, uint64_t& len) {
+            const int o = tile_order[k].first;
+            off = start[o] + tile_order[k].second * T;
+            len = std::min(T, start[o + 1] - off);
+            return o;
+          };
+          while (r < nr || c < nr) {
+            const uint64_t pos = pieces.size();
+            const bool can_c = c < r && rpos[c] + D + 1 <= pos;
+            uint64_t oa = 0, la = 0, ob = 0, lb = 0;
+            int a_own = r < nr ? tile(r, oa, la) : 0;
+            int b_own = c < nr ? tile(c, ob, lb) : 0;
+            bool coaligned = true;
+            for (int d = 0; d < world; ++d)
+              if (d != b_own && ((dst_res[d] + ob) & 15u) != ((dst_res[b_own == 0 ? 1 : 0] + ob) & 15u)) coaligned = false;
+            if (can_c && r < nr && la == lb && coaligned) {
+              rpos[r] = pos;
+              pieces.push_back(Piece{oa, ob, la, ALL | (1u << (16 + b_own)), (1u << a_own) | kFused,
+                                     (uint32_t)(b_own * tmax + tile_order[c].second + 1),
+                                     (uint32_t)(a_own * tmax + tile_order[r].second + 1)});
+              ++r;
+              ++c;
+            } else if (r < nr && !can_c) {
+              rpos[r] = pos;
+              reduce_piece(tile_order[r].first, tile_order[r].second);
+              ++r;
+            } else {
+              copy_piece(tile_order[c].first, tile_order[c].second);
+              ++c;
+            }
+          }
+        } else
         while (r < nr || c < nr) {
           const uint64_t pos = pieces.size();
           const bool want_r = (((pos / G) + (pos % G)) & 1u) == 0;
@@ -552,7 +596,7 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
       } else {
         // one rank: every layout is the one-shot copy (and the two-shot's L2
         // priorities have no copies to serve)
-        if (p.tune.layout == kTwoShot && p.tune.store_hint == 3) p.tune.store_hint = 1;
+        if ((p.tune.layout == kTwoShot || p.tune.layout == kTwoShotFused) && p.tune.store_hint == 3) p.tune.store_hint = 1;
         p.tune.layout = kOneShot;
         push_grouped(pieces, Piece{0, 0, S, ALL, ALL, 0, 0}, dst_res);
       }
@@ -675,7 +719,8 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
   // store_hint 3 keeps reduce results evict-last in the L2 until a copy has
   // read them back: only the two-shot layout (register path) has such copies
   if (p.tune.store_hint == 3 &&
-      !(coll == kAllReduce && p.tune.layout == kTwoShot && sync && p.tune.path == kPathRegister))
+      !(coll == kAllReduce && (p.tune.layout == kTwoShot || p.tune.layout == kTwoShotFused) && sync &&
+        p.tune.path == kPathRegister))
     return PL_ERR_INVALID_ARG;
   if (!p.reduce) p.nsrc = 1;
   // the register-path kernel for more than 8 sources is built for CTAs of at
@@ -824,11 +869,37 @@ std::string check_plan(const Plan& p) {
     if (it.len == 0) return "empty item";
     const uint32_t in_bits = it.src_mask & 0xFFFFu, out_bits = it.src_mask >> 16;
     const uint32_t dst_bits = it.dst_mask & kDstRanks, split = it.dst_mask & (kSplitSrc | kSplitDst);
+    const bool fused = (it.dst_mask & kFused) != 0;
     if ((in_bits & ~ALL) || (out_bits & ~ALL)) return "source mask outside the world";
-    if (!dst_bits || (dst_bits & ~ALL) || (it.dst_mask & ~(kDstRanks | kSplitSrc | kSplitDst)))
+    if (!dst_bits || (dst_bits & ~ALL) || (it.dst_mask & ~(kDstRanks | kSplitSrc | kSplitDst | kFused)))
       return "destination mask empty or outside the world";
     const int nsrc = popcount32(it.src_mask);
     if (nsrc < 1) return "item without a source";
+    if (fused) {
+      // reduce the tile at src_off into the destination, copy the tile at
+      // dst_off from the output source to every other output
+      if (p.tune.layout != kTwoShotFused || split || popcount32(out_bits) != 1 || popcount32(dst_bits) != 1 ||
+          popcount32(in_bits) < 2 || !it.wait || !it.notify)
+        return "a fused item outside the two-shot layout";
+      if ((it.src_off | it.dst_off | it.len) % (uint64_t)p.elem) return "reduce not element aligned";
+      for (uint32_t m = in_bits; m; m &= m - 1)
+        if (it.src_off + it.len > p.in_bytes[__builtin_ctz(m)]) return "a fused item reads past an input";
+      const int ob = __builtin_ctz(out_bits), oa = __builtin_ctz(dst_bits);
+      if (it.dst_off + it.len > p.out_bytes[ob] || it.src_off + it.len > p.out_bytes[oa])
+        return "a fused item reaches past an output";
+      acc[oa].push_back({it.src_off, it.src_off + it.len, (int64_t)i, true});
+      acc[ob].push_back({it.dst_off, it.dst_off + it.len, (int64_t)i, false});
+      for (int d = 0; d < p.world; ++d)
+        if (d != ob) {
+          if (it.dst_off + it.len > p.out_bytes[d]) return "a fused item writes past an output";
+          acc[d].push_back({it.dst_off, it.dst_off + it.len, (int64_t)i, true});
+        }
+      if (it.wait > (uint32_t)p.n_flags) return "wait flag out of range";
+      const int64_t at = notified_at[it.wait - 1];
+      if (at < 0) return "wait without a notify";
+      if ((p.strided || p.queue) && at >= (int64_t)i) return "wait without an earlier notify";
+      continue;
+    }
     if (split) {
       // the ring's binary32 running sum over bf16 data: two output halves in
       // neighbouring ranks, read and / or written by one reduce item

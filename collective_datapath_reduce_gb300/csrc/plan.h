@@ -36,7 +36,7 @@ enum Coll : int {
 
 enum Dtype : int { kU8 = 0, kF32 = 1, kBF16 = 2 };
 
-enum Layout : int { kLayoutAuto = 0, kOneShot = 1, kTwoShot = 2, kRing = 3 };
+enum Layout : int { kLayoutAuto = 0, kOneShot = 1, kTwoShot = 2, kRing = 3, kTwoShotFused = 4 };
 
 enum Path : int { kPathRegister = 1, kPathBulk = 2 };
 
@@ -69,6 +69,12 @@ static_assert(sizeof(Item) == 40, "device item layout");
 // sum instead of a rounded bf16 value.  Only the ring kernel reads them.
 constexpr uint32_t kSplitSrc = 1u << 30;
 constexpr uint32_t kSplitDst = 1u << 31;
+// Two-shot AllReduce with L2 priorities: one item reduces the tile at src_off
+// (sources: the item's input bits; destination: its one destination bit) and,
+// in the same pass, copies the tile at dst_off from the output named by its
+// output source bit to every other rank's output.  It notifies the flag of
+// the tile it reduces and waits for the flag of the tile it copies.
+constexpr uint32_t kFused = 1u << 29;
 constexpr uint32_t kDstRanks = 0xFFFFu;
 
 struct Tune {

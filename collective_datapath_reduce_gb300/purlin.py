@@ -40,7 +40,7 @@ PL_COLL_REDUCE_SCATTER_V = 6
 PL_COLL_ATOM_COPY = 7
 PL_COLL_ATOM_REDUCE = 8
 
-PL_LAYOUT_AUTO, PL_LAYOUT_ONE_SHOT, PL_LAYOUT_TWO_SHOT, PL_LAYOUT_RING = 0, 1, 2, 3
+PL_LAYOUT_AUTO, PL_LAYOUT_ONE_SHOT, PL_LAYOUT_TWO_SHOT, PL_LAYOUT_RING, PL_LAYOUT_TWO_SHOT_FUSED = 0, 1, 2, 3, 4
 PATH_REGISTER, PATH_BULK = 1, 2
 PL_SCHED_ITEM, PL_SCHED_STREAM, PL_SCHED_QUEUE, PL_SCHED_QUEUE_GUIDED = 1, 2, 3, 4
 

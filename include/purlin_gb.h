@@ -118,7 +118,14 @@ typedef enum {
   PL_LAYOUT_AUTO = 0,
   PL_LAYOUT_ONE_SHOT = 1,
   PL_LAYOUT_TWO_SHOT = 2,
-  PL_LAYOUT_RING = 3
+  PL_LAYOUT_RING = 3,
+  /* The two-shot layout with fused items: after a first wave of reduces, each
+   * item reduces one owner tile and, in the same pass, copies a tile another
+   * CTA reduced one wave earlier (its SNAC wait), so every CTA streams the
+   * one-shot layout's mix of reads and writes.  Same results.  Register path,
+   * item schedule and store_hint 3 only (PL_ERR_UNSUPPORTED otherwise); only on
+   * request. */
+  PL_LAYOUT_TWO_SHOT_FUSED = 4
 } purlin_layout;
 
 /* Tuning of one call (the role of Purlin's host tuning policies).  A zero field
@@ -179,7 +186,12 @@ typedef struct {
                         kept as two 16-bit halves in two neighbouring ranks' outputs (low
                         half in the lower rank): bit 30, the item's two output sources are
                         those halves; bit 31, its two destinations receive the halves of
-                        the new sum instead of a rounded bf16 value. */
+                        the new sum instead of a rounded bf16 value.  Bit 29 marks a fused
+                        two-shot item: it reduces the tile at src_off (its input bits) into
+                        the output of its one destination bit and, in the same pass, copies
+                        the tile at dst_off from the output of its output source bit to
+                        every other rank's output; it notifies the flag of the tile it
+                        reduces and waits for the flag of the tile it copies. */
   uint32_t wait;     /* 0, or 1 + index of the SNAC flag consumed before the item */
   uint32_t notify;   /* 0, or 1 + index of the SNAC flag raised after the item */
   uint32_t cta;      /* CTA that runs the item; 0xFFFFFFFF under PL_SCHED_QUEUE (any CTA) */

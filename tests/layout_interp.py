@@ -15,7 +15,7 @@ import numpy as np
 
 import oracle
 
-SPLIT_SRC, SPLIT_DST = 1 << 30, 1 << 31
+SPLIT_SRC, SPLIT_DST, FUSED = 1 << 30, 1 << 31, 1 << 29
 
 
 QUEUED = 0xFFFFFFFF
@@ -55,9 +55,28 @@ def run_items(items, ins, outs, dtype, as_given=False):
     """ins / outs: lists of uint8 arrays (rank buffers as bytes).  Items are
     applied in an order the CTAs could run them (schedule()), or as given
     (as_given: the caller orders them)."""
+    world = len(outs)
     for it in (items if as_given else schedule(items)):
         n = int(it["len"])
         so, do = int(it["src_off"]), int(it["dst_off"])
+        if it["dst_mask"] & FUSED:
+            # two-shot fused item: reduce the tile at src_off into the
+            # destination bit's output, copy the tile at dst_off from the
+            # output source bit to every other output
+            ranks = [r for r in range(16) if (it["src_mask"] >> r) & 1]
+            ob = [r for r in range(16) if (it["src_mask"] >> (16 + r)) & 1][0]
+            oa = [r for r in range(16) if (it["dst_mask"] >> r) & 1][0]
+            tile = outs[ob][do:do + n].copy()
+            if dtype == "f32":
+                acc = oracle.fold_sum([ins[r][so:so + n].view(np.float32) for r in ranks])
+                outs[oa][so:so + n] = acc.view(np.uint8)
+            else:
+                acc = oracle.fold_sum([oracle.bf16_bits_to_f32(ins[r][so:so + n].view(np.uint16)) for r in ranks])
+                outs[oa][so:so + n] = oracle.f32_to_bf16_rne(acc).view(np.uint8)
+            for d in range(world):
+                if d != ob:
+                    outs[d][do:do + n] = tile
+            continue
         srcs = []
         m = it["src_mask"]
         b = 0

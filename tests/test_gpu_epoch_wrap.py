@@ -38,6 +38,7 @@ TUNES = [
     ("two_shot_bulk", {"layout": P.PL_LAYOUT_TWO_SHOT, "chunk_bytes": 4096, "path": P.PATH_BULK, "stages": 2},
      oracle.all_reduce),
     ("ring", {"layout": P.PL_LAYOUT_RING, "chunk_bytes": 16384}, oracle.all_reduce),
+    ("two_shot_fused", {"layout": P.PL_LAYOUT_TWO_SHOT_FUSED, "chunk_bytes": 4096}, oracle.all_reduce),
 ]
 
 

@@ -60,7 +60,7 @@ SMS = [1, 7, 152]
 
 @pytest.mark.parametrize("world", [1, 2, 3, 8, 16])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("layout", [P.PL_LAYOUT_ONE_SHOT, P.PL_LAYOUT_TWO_SHOT])
+@pytest.mark.parametrize("layout", [P.PL_LAYOUT_ONE_SHOT, P.PL_LAYOUT_TWO_SHOT, P.PL_LAYOUT_TWO_SHOT_FUSED])
 def test_all_reduce_plan(world, dtype, layout):
     E = ESZ[dtype]
     for n in (1, 7, 1000, 4096 + 3):
@@ -76,7 +76,7 @@ def test_all_reduce_plan(world, dtype, layout):
             want = oracle.all_reduce(ins, dtype)
             for r in range(world):
                 assert np.array_equal(outs[r], _bytes(want[r])), (n, sm, r)
-            if layout == P.PL_LAYOUT_TWO_SHOT and world > 1:
+            if layout in (P.PL_LAYOUT_TWO_SHOT, P.PL_LAYOUT_TWO_SHOT_FUSED) and world > 1:
                 assert nflags > 0
                 notify_at, kinds = {}, {}
                 for i, it in enumerate(items):
@@ -87,10 +87,16 @@ def test_all_reduce_plan(world, dtype, layout):
                         # increasing global order (item i on CTA i % grid)
                         assert notify_at[it["wait"]] < i
                     assert it["cta"] == i % grid
-                    kinds.setdefault(it["cta"], set()).add(popcount(it["src_mask"]) > 1)
+                    if it["dst_mask"] & (1 << 29):
+                        # fused: reduces one tile, copies one another CTA reduced
+                        assert it["wait"] and it["notify"] and it["wait"] != it["notify"]
+                        assert items[notify_at[it["wait"]]]["cta"] != it["cta"]
+                        kinds.setdefault(it["cta"], set()).update({True, False})
+                    else:
+                        kinds.setdefault(it["cta"], set()).add(popcount(it["src_mask"]) > 1)
                 if len(items) >= 4 * grid and len(set(dres)) == 1:
-                    # reduces and copies alternate on every CTA (none runs only
-                    # one kind; copies split by destination alignment shift it)
+                    # every CTA reduces and copies (none runs only one kind;
+                    # copies split by destination alignment shift the order)
                     assert all(k == {True, False} for k in kinds.values())
 
 
@@ -490,3 +496,31 @@ def test_default_workspace_holds_the_snac_layouts_flags():
             assert st == P.PL_OK
             assert nflags <= default, (world, S, layout, nflags)
             assert P.purlin_workspace_bytes(world, S) >= 256 + 4 * nflags
+
+
+@pytest.mark.parametrize("world", [2, 3, 8, 16])
+def test_two_shot_fused_items(world):
+    """The fused two-shot layout: after a first wave of reduces, items reduce
+    one tile and copy another that a different CTA reduced at least a wave
+    earlier; results equal the oracle's; it runs only with store_hint 3 on
+    the register path's item schedule."""
+    for n, sm in ((300007, 7), (65536 * world + 5, 3), (1000, 152)):
+        ins = [_draw("bf16", n) for _ in range(world)]
+        tune = {"layout": P.PL_LAYOUT_TWO_SHOT_FUSED, "chunk_bytes": 4096}
+        items, grid, _ = _describe(P.PL_COLL_ALL_REDUCE, world, P.PL_BF16, [n * 2], sm=sm, tune=tune)
+        outs = [np.zeros(n * 2, np.uint8) for _ in range(world)]
+        run_items(items, [_bytes(x) for x in ins], outs, "bf16")
+        want = oracle.all_reduce(ins, "bf16")
+        for r in range(world):
+            assert np.array_equal(outs[r], _bytes(want[r])), (n, sm, r)
+        at = {it["notify"]: i for i, it in enumerate(items) if it["notify"]}
+        fused = [i for i, it in enumerate(items) if it["dst_mask"] & (1 << 29)]
+        if len(items) > 3 * grid:
+            assert fused, "long plans fuse"
+        for i in fused:
+            j = at[items[i]["wait"]]
+            assert j < i and i - j > grid and items[j]["cta"] != items[i]["cta"]
+    for bad in ({"store_hint": 1}, {"schedule": P.PL_SCHED_QUEUE}, {"path": P.PATH_BULK}):
+        st, *_ = P.purlin_plan_describe(P.PL_COLL_ALL_REDUCE, world, P.PL_BF16, [1 << 20], None, None, 152,
+                                        dict({"layout": P.PL_LAYOUT_TWO_SHOT_FUSED}, **bad))
+        assert st == P.PL_ERR_UNSUPPORTED, bad

@@ -69,7 +69,8 @@ def _lib():
 
 @SETTINGS
 @given(world=st.integers(1, 16), n=st.integers(0, 3000), dtype=st.sampled_from(["f32", "bf16"]),
-       layout=st.sampled_from([P.PL_LAYOUT_ONE_SHOT, P.PL_LAYOUT_TWO_SHOT, P.PL_LAYOUT_RING]),
+       layout=st.sampled_from([P.PL_LAYOUT_ONE_SHOT, P.PL_LAYOUT_TWO_SHOT, P.PL_LAYOUT_RING,
+                              P.PL_LAYOUT_TWO_SHOT_FUSED]),
        sm=st.integers(1, 160), tune=tunes(), seed=st.integers(0, 2**32 - 1), data=st.data())
 def test_all_reduce_plans(world, n, dtype, layout, sm, tune, seed, data):
     E = ESZ[dtype]
