@@ -5,7 +5,9 @@ The layouts cut every piece into items of at most 1 GiB (the Atoms count
 each kind of kernel over buffers of 2.25 to 4.5 GiB per rank, with ragged
 sizes, in the default launch configuration:
 
-* AllReduce bf16, 2 ranks x 2.5 GiB (+6 bytes), one-shot, two-shot and ring;
+* AllReduce bf16, 2 ranks x 2.5 GiB (+6 bytes), one-shot, two-shot, fused
+  two-shot and ring; 3 ranks x 2.25 GiB (+6 bytes), ring (whose running sum
+  then crosses stages as two 16-bit halves) and fused two-shot;
 * ReduceScatter fp32, 2 ranks x 2.5 GiB (bulk path, 1.25 GiB outputs);
 * AllGather u8, 2 ranks x 2.25 GiB (+5 bytes): outputs of 4.5 GiB, the second
   block at an odd offset;
@@ -95,7 +97,8 @@ def ar_inputs():
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("layout", [P.PL_LAYOUT_AUTO, P.PL_LAYOUT_TWO_SHOT, P.PL_LAYOUT_RING])
+@pytest.mark.parametrize("layout", [P.PL_LAYOUT_AUTO, P.PL_LAYOUT_TWO_SHOT, P.PL_LAYOUT_TWO_SHOT_FUSED,
+                                    P.PL_LAYOUT_RING])
 def test_all_reduce_2x2_5GiB(ar_inputs, layout):
     S, n, T, src = ar_inputs
     dst = RankBuffers([S] * 2)
@@ -111,6 +114,32 @@ def test_all_reduce_2x2_5GiB(ar_inputs, layout):
     for r in range(2):
         assert np.array_equal(sample(dst, r, "bf16", pos), want[r]), r
     assert dst.guards_intact() and src.guards_intact()
+
+
+@pytest.mark.parametrize("layout", [P.PL_LAYOUT_RING, P.PL_LAYOUT_TWO_SHOT_FUSED])
+def test_all_reduce_3x2_25GiB(layout):
+    """Three ranks: the ring's bf16 running sum travels as two 16-bit halves
+    in the outputs, at offsets past 2^31 and 2^32 bytes."""
+    world, S = 3, 9 * GiB // 4 + 6
+    n = S // 2
+    T = [Tiled(n, "bf16", seed=31 + r, shift=777 * r) for r in range(world)]
+    src = RankBuffers([S] * world)
+    for r in range(world):
+        upload(src, r, T[r])
+    dst = RankBuffers([S] * world)
+    h = Handle(world)
+    P.check(P.purlin_tune_override(h.h, {"layout": layout}))
+    P.check(P.purlin_all_reduce(h.h, src.ptrs(), dst.ptrs(), S, P.PL_BF16, 0, stream()))
+    sync()
+    assert h.status() == 0 and h.close() == P.PL_OK
+    assert torch.equal(dst.view(0), dst.view(1)) and torch.equal(dst.view(0), dst.view(2))
+    pos = positions(n, 2, seed=37)
+    want = oracle.all_reduce([t.at(pos) for t in T], "bf16")
+    for r in range(world):
+        assert np.array_equal(sample(dst, r, "bf16", pos), want[r]), r
+    assert dst.guards_intact() and src.guards_intact()
+    del src, dst
+    torch.cuda.empty_cache()
 
 
 def test_reduce_scatter_f32_2x2_5GiB():
