@@ -82,7 +82,8 @@ def test_checks_are_silent_on_correct_calls(checking, name, tune):
                                   {"path": P.PATH_BULK},
                                   {"path": P.PATH_BULK, "schedule": P.PL_SCHED_QUEUE, "interleave_bytes": 8192},
                                   {"path": P.PATH_REGISTER, "layout": P.PL_LAYOUT_TWO_SHOT, "chunk_bytes": 4096},
-                                  {"path": P.PATH_REGISTER, "layout": P.PL_LAYOUT_RING, "chunk_bytes": 4096}])
+                                  {"path": P.PATH_REGISTER, "layout": P.PL_LAYOUT_RING, "chunk_bytes": 4096},
+                                  {"path": P.PATH_REGISTER, "layout": P.PL_LAYOUT_TWO_SHOT_FUSED, "chunk_bytes": 4096}])
 def test_limited_output_is_caught(checking, tune):
     world = 4
     n = 4 * 40000
