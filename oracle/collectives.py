@@ -12,8 +12,7 @@ Sources, by page and section:
          copy and N-to-1 reduce.  "Reduction determinism": deterministic mode
          gives bit-repeatable results for the same inputs.
 
-Readings taken where the pages leave a step open (each is also listed in the
-design notes of the repository):
+Readings taken where the pages leave a step open:
   * Reductions accumulate in IEEE binary32, as a left fold in ascending rank
     order that starts from rank 0's value (not from +0.0), one rounding per add;
     bf16 results are rounded once, at the end, to nearest with ties to even.
