@@ -291,8 +291,11 @@ __device__ __forceinline__ void st_vec_policy(void* p, uint4 v, uint64_t pol) {
                : "memory");
 }
 
+// Return the 128-byte line that starts at p to normal L2 priority; any other
+// p (inside a line) does nothing, so that each line is demoted once, by the
+// thread that read its first 16 bytes, at the line's own address.
 __device__ __forceinline__ void l2_priority_normal(const void* p) {
-  asm volatile("applypriority.global.L2::evict_normal [%0], 128;" ::"l"(p) : "memory");
+  if (((uintptr_t)p & 127u) == 0) asm volatile("applypriority.global.L2::evict_normal [%0], 128;" ::"l"(p) : "memory");
 }
 
 __device__ __forceinline__ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
@@ -351,8 +354,8 @@ __device__ __forceinline__ void copy_owner_tile(const char* src, char* const* ds
   uint32_t v = threadIdx.x;
   for (; v + step < nv; v += 2 * step) {
     const uint4 r0 = ld_l2(s4 + v), r1 = ld_l2(s4 + v + step);
-    if ((v & 7u) == 0) l2_priority_normal(s4 + v);
-    if (((v + step) & 7u) == 0) l2_priority_normal(s4 + v + step);
+    l2_priority_normal(s4 + v);
+    l2_priority_normal(s4 + v + step);
     for (int j = 0; j < nd; ++j) {
       uint4* d4 = reinterpret_cast<uint4*>(dst[j]);
       st_vec<true>(d4 + v, r0);
@@ -361,7 +364,7 @@ __device__ __forceinline__ void copy_owner_tile(const char* src, char* const* ds
   }
   for (; v < nv; v += step) {
     const uint4 r = ld_l2(s4 + v);
-    if ((v & 7u) == 0) l2_priority_normal(s4 + v);
+    l2_priority_normal(s4 + v);
     for (int j = 0; j < nd; ++j) st_vec<true>(reinterpret_cast<uint4*>(dst[j]) + v, r);
   }
 }
@@ -389,7 +392,7 @@ __device__ __forceinline__ void fused_owner_tiles(const char* const* src, int ns
 #pragma unroll
         for (int b = 0; b < NS; ++b) r[b] = ld_stream_policy(reinterpret_cast<const uint4*>(src[b]) + v, pf);
         const uint4 y = ld_l2(sb + v);
-        if ((v & 7u) == 0) l2_priority_normal(sb + v);
+        l2_priority_normal(sb + v);
         float acc[EPV];
 #pragma unroll
         for (int e = 0; e < EPV; ++e) acc[e] = Elem<T>::get(r[0], e);
