@@ -25,7 +25,7 @@ namespace {
 
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 // Library-owned workspace: flags for the two-shot and ring AllReduce layouts
-// at the table's tile sizes up to several GiB per rank (4 MiB of flags).
+// at the table's tile sizes up to several GiB per rank (8 MiB of flags).
 constexpr size_t kDefaultFlags = PURLIN_DEFAULT_WORKSPACE_FLAGS;
 
 struct DevPlan {

@@ -329,12 +329,10 @@ Tune resolve_tune(int coll, int table_coll, int world, int dtype, uint64_t bytes
       t.store_hint = ((t.layout == kTwoShot || t.layout == kTwoShotFused) && t.path == kPathRegister) ? 3 : 1;
     if (!over.max_ctas) t.max_ctas = 0;
     if (t.layout == kRing && !over.unroll) t.unroll = 2;
-    if (t.layout == kRing && !over.chunk_bytes) {
-      // ring tiles of a 64th of a chunk, 64-128 KiB (graph of 10 calls, 8
-      // ranks: 64 KiB best at 16 MiB per rank, 95 against 129 us for 128 KiB;
-      // 128 KiB best at 64 MiB, 355 against 391 us for 64 KiB)
-      const uint64_t tile = bytes_per_rank / (uint64_t)std::max(world, 1) / 64 / 16 * 16;
-      t.chunk_bytes = (int)std::min<uint64_t>(128 * 1024, std::max<uint64_t>(64 * 1024, tile));
+    if (t.layout == kRing) {
+      // ring: tiles of 64 KiB (8 ranks, back to back, stages one wave apart:
+      // 404.9 against 444.9 us for 128 KiB at 8 x 64 MiB)
+      if (!over.chunk_bytes) t.chunk_bytes = 64 * 1024;
     }
   }
   return t;
@@ -555,9 +553,11 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
         };
         const uint64_t gcap = (uint64_t)p.tune.ctas_per_sm * sm_count;
         const uint64_t G = std::max<uint64_t>(1, std::min<uint64_t>(gcap, n_items));
-        // stage st of tile t is emitted `lag` tile steps after stage st - 1, so
-        // about one wave of CTAs separates a flag's notify from its wait
-        const uint64_t lag = std::max<uint64_t>(1, ceil_div(G, (uint64_t)world));
+        // A tile's stage comes at least D = snac_lag x G / 2 places (one
+        // wave of CTAs by default) after its previous stage in the items'
+        // order: the previous stage has usually finished, and the running
+        // sum is read back while it is still in the L2.
+        const uint64_t D = std::max<uint64_t>(1, (uint64_t)p.tune.snac_lag * G / 2);
         auto stage_piece = [&](int j, uint64_t t, uint32_t st) {
           const uint64_t off = start[j] + t * T, len = std::min(T, start[j + 1] - off);
           uint32_t src, dst;
@@ -585,14 +585,46 @@ int build_plan(int coll, int world, int dtype, const uint64_t* sizes, size_t nsi
             push_grouped(pieces, q, dst_res);
           }
         };
-        for (uint64_t step = 0; step < tmax + (uint64_t)(stages - 1) * lag; ++step)
-          for (uint32_t st = 0; st < stages; ++st) {
-            if (step < (uint64_t)st * lag) break;
-            const uint64_t t = step - (uint64_t)st * lag;
-            if (t >= tmax) continue;
-            for (int j = 0; j < world; ++j)
-              if (t < tiles[j]) stage_piece(j, t, st);
+        // Emission: at every place, the oldest pending stage if it is due,
+        // else the first stage of the next tile (tile-major over the chunks),
+        // else the oldest pending stage anyway (it will wait for its flag).
+        // Stages become due in the order they were queued, so a FIFO holds
+        // them in due order.
+        struct Pending {
+          uint64_t due;
+          int j;
+          uint64_t t;
+          uint32_t st;
+        };
+        std::vector<Pending> fifo;
+        size_t head = 0;
+        uint64_t next_t = 0;
+        int next_j = 0;
+        auto advance_new = [&]() {  // the next (chunk, tile) that exists
+          while (next_t < tmax && (uint64_t)tiles[next_j] <= next_t) {
+            if (++next_j == world) {
+              next_j = 0;
+              ++next_t;
+            }
           }
+        };
+        advance_new();
+        while (head < fifo.size() || next_t < tmax) {
+          const uint64_t pos = pieces.size();
+          Pending e;
+          if (head < fifo.size() && (fifo[head].due <= pos || next_t >= tmax)) {
+            e = fifo[head++];
+          } else {
+            e = Pending{0, next_j, next_t, 0};
+            if (++next_j == world) {
+              next_j = 0;
+              ++next_t;
+            }
+            advance_new();
+          }
+          stage_piece(e.j, e.t, e.st);
+          if (e.st + 1 < stages) fifo.push_back(Pending{pieces.size() - 1 + D, e.j, e.t, e.st + 1});
+        }
       } else {
         // one rank: every layout is the one-shot copy (and the two-shot's L2
         // priorities have no copies to serve)

@@ -61,10 +61,10 @@ extern "C" {
 
 #define PURLIN_MAX_WORLD 16
 /* SNAC flags of the workspace the library allocates when purlin_initialize is
- * given none (4 MiB of flags): the two-shot and ring AllReduce layouts at the
+ * given none (8 MiB of flags): the two-shot and ring AllReduce layouts at the
  * tuning table's tile sizes for up to 8 ranks of about 9 GiB each, or 16
  * ranks of about 4 GiB. */
-#define PURLIN_DEFAULT_WORKSPACE_FLAGS 1048576u
+#define PURLIN_DEFAULT_WORKSPACE_FLAGS 2097152u
 
 typedef struct purlin_ctx* purlin_handle;
 typedef void* purlin_stream_t; /* a cudaStream_t */
@@ -151,9 +151,9 @@ typedef struct {
                            contiguous share per CTA (0 = the table's choice) */
   int max_ctas;     /* > 0: at most this many CTAs (fewer concurrent DRAM streams) */
   int schedule;     /* purlin_schedule: how CTAs walk their items */
-  int snac_lag;     /* two-shot AllReduce: a tile's copies come at least snac_lag x grid / 2
-                       places after its reduce in the items' order (1..64; table: 4, two
-                       waves of CTAs) */
+  int snac_lag;     /* two-shot and ring AllReduce: a flag's consumer comes about snac_lag x
+                       grid / 2 places after its producer in the items' order (1..64;
+                       table: 2, one wave of CTAs) */
 } purlin_tune;
 
 /* How the CTAs of a launch walk the plan's work items (purlin_tune.schedule).

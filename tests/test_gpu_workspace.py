@@ -48,7 +48,7 @@ def test_snac_layouts_at_the_workload_size_do_not_grow_it():
     h = Handle(world)
     try:
         st, nbytes, grown = P.purlin_workspace_query(h.h)
-        assert st == P.PL_OK and grown == 0 and nbytes >= 256 + 4 * (1 << 20)
+        assert st == P.PL_OK and grown == 0 and nbytes >= 256 + 4 * (2 << 20)
         for layout in (P.PL_LAYOUT_TWO_SHOT, P.PL_LAYOUT_RING):
             outs = _run(h, world, ins, {"layout": layout})
             for r in range(world):
@@ -71,9 +71,9 @@ def test_initialize_takes_a_size_for_its_own_workspace():
 
 
 def test_past_the_capacity_it_grows_once_and_stays_exact():
-    """16 ranks x 40 MiB, ring tiles of 1 KiB: about 1.19 million flags, more
-    than the default 1 Mi; the call grows the workspace once."""
-    world, n = 16, 20 << 20
+    """16 ranks x 80 MiB, ring tiles of 1 KiB: about 2.4 million flags, more
+    than the default 2 Mi; the call grows the workspace once."""
+    world, n = 16, 40 << 20
     rng = np.random.default_rng(17)
     ins = [inputs.to_bf16_bits(rng.standard_normal(n).astype(np.float32)) for _ in range(world)]
     h = Handle(world)

@@ -189,15 +189,34 @@ def test_ring_all_reduce_plan(world, dtype):
 
 
 def test_ring_tiles_follow_the_chunk_size():
-    """Ring tiles are a 64th of a chunk, between 64 and 128 KiB, unless the caller sets chunk_bytes."""
+    """Ring tiles are 64 KiB unless the caller sets chunk_bytes."""
     MI = 1 << 20
-    for world, S, tile in ((8, 1 * MI, 65536), (8, 16 * MI, 65536), (8, 48 * MI, 98304), (8, 64 * MI, 131072),
-                           (8, 256 * MI, 131072), (16, 64 * MI, 65536), (2, 16 * MI, 131072)):
+    for world, S in ((8, 1 * MI), (8, 16 * MI), (8, 64 * MI), (8, 256 * MI), (16, 64 * MI), (2, 16 * MI)):
         items, _, _ = _describe(P.PL_COLL_ALL_REDUCE, world, P.PL_BF16, [S], tune={"layout": P.PL_LAYOUT_RING})
-        assert max(int(it["len"]) for it in items) == min(tile, S // world), (world, S)
+        assert max(int(it["len"]) for it in items) == min(65536, S // world), (world, S)
     items, _, _ = _describe(P.PL_COLL_ALL_REDUCE, 8, P.PL_BF16, [64 * MI],
                             tune={"layout": P.PL_LAYOUT_RING, "chunk_bytes": 32768})
     assert max(int(it["len"]) for it in items) == 32768
+
+
+def test_ring_stages_one_wave_apart():
+    """A tile's consecutive stages sit about snac_lag x grid / 2 places apart in
+    the items' order (one wave of CTAs by default) while other tiles' stages
+    can fill the places in between, and as far apart as the tiles allow when
+    they cannot."""
+    MI = 1 << 20
+    for S in (4 * MI, 16 * MI, 64 * MI):
+        for lag in (2, 6):
+            items, grid, _ = _describe(P.PL_COLL_ALL_REDUCE, 8, P.PL_BF16, [S],
+                                       tune={"layout": P.PL_LAYOUT_RING, "snac_lag": lag})
+            at = {it["notify"]: i for i, it in enumerate(items) if it["notify"]}
+            gaps = sorted(i - at[it["wait"]] for i, it in enumerate(items) if it["wait"])
+            D = lag * grid // 2
+            n_tiles = sum(1 for it in items if not it["wait"])   # first stages
+            med = gaps[len(gaps) // 2]
+            # with fewer tiles than D places, every tile's next stage comes
+            # after the same stage of all the others
+            assert min(D, n_tiles) <= med <= 2 * D, (S, lag, med, D, n_tiles)
 
 
 @pytest.mark.parametrize("world", [2, 4])
