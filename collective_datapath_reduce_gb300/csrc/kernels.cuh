@@ -32,6 +32,23 @@
 
 namespace pl {
 
+// ------------------------------------------------- item prefetch
+
+// Copy work item `src` (global memory, 8-byte aligned) into shared memory
+// `dst` with asynchronous 8-byte copies, so no register holds it while the
+// CTA moves the current item.  The issuing thread calls item_prefetch_wait()
+// before it reads `dst`.
+__device__ __forceinline__ void item_prefetch(Item* dst, const Item* src) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+#pragma unroll
+  for (int k = 0; k < (int)(sizeof(Item) / 8); ++k)
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(d + 8 * k), "l"(reinterpret_cast<const char*>(src) + 8 * k)
+                 : "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void item_prefetch_wait() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // --------------------------------------------------------- the SNAC loop
 
 // Spin until *flag == epoch.  Thread 0 only.  Gives up when the time limit
@@ -472,6 +489,7 @@ __global__ void __launch_bounds__(snac_max_threads<NS>(), 2) snac_kernel(const _
   __shared__ uint32_t s_item, s_notify, s_epoch, s_wait_ns, s_split;
   __shared__ const char* s_fsrc;  // fused items: the copied tile
   __shared__ uint32_t s_next_i, s_q_i;  // thread 0's item cursor (kept out of the registers of the Atoms)
+  __shared__ __align__(16) Item s_next;  // the next item, prefetched by thread 0
   __shared__ unsigned long long s_t0;
   grid_dep_wait();
 
@@ -491,14 +509,13 @@ __global__ void __launch_bounds__(snac_max_threads<NS>(), 2) snac_kernel(const _
   }
   if (threadIdx.x == 0) s_epoch = a.sync ? ld_volatile(&a.ctl[kCtlEpoch]) + 1u : 0u;
 
-  // Thread 0 keeps the next item in registers so its load overlaps the
-  // current one (and, on the queue, the index fetched for the item after it).
-  Item next;
+  // Thread 0 copies the next item into shared memory while the CTA moves the
+  // current one (and, on the queue, fetches the index of the item after it).
   if (threadIdx.x == 0) {
     s_next_i = begin;
     s_q_i = 0;
     if (begin < end) {
-      next = a.items[begin];
+      item_prefetch(&s_next, a.items + begin);
       if (a.queue) s_q_i = gridDim.x + atomicAdd(&a.ctl[kCtlQueue], 1u);
     }
   }
@@ -507,11 +524,12 @@ __global__ void __launch_bounds__(snac_max_threads<NS>(), 2) snac_kernel(const _
       s_item = kNoItem;
       const uint32_t i = s_next_i;
       if (i < end) {
-        const Item it = next;
+        item_prefetch_wait();
+        const Item it = s_next;
         const uint32_t ni = a.queue ? s_q_i : i + step;
         s_next_i = ni;
         if (ni < end) {
-          next = a.items[ni];
+          item_prefetch(&s_next, a.items + ni);
           if (a.queue) s_q_i = gridDim.x + atomicAdd(&a.ctl[kCtlQueue], 1u);
         }
         s_item = i;

@@ -47,8 +47,7 @@ struct NaArgs {
   uint32_t world;
   uint32_t tmax;             // tiles of the largest owner range
   uint32_t half;             // reduce slots (and copy slots) per wave: grid / 2
-  uint32_t lag;              // copy slots before the first copy: one wave
-  uint32_t slots;            // waves x grid
+  uint32_t slots;            // positions of the order: a reduce and a copy per tile
   uint32_t dst_coaligned;    // every output has the same address residue mod 16
   uint32_t drop_notify;      // test hook: 1 + flag whose notify is skipped, or 0
 };
@@ -83,23 +82,34 @@ __global__ void __launch_bounds__(kNaThreads, 2) noalloc_kernel(const __grid_con
   const uint32_t N = a.world;
   const uint32_t G = gridDim.x, c = blockIdx.x;
   if (threadIdx.x == 0) s_epoch = ld_volatile(a.scratch + kNaEpoch) + 1u;
-  // Slot s runs on CTA s % G in increasing order.  Reduce and copy slots
-  // alternate in a checkerboard of (wave s / G, CTA): every CTA alternates
-  // the two kinds, and each wave holds `half` of each.  Reduce slot k takes
-  // tile k (tile-major over the owners); copy slot k takes tile k - lag, one
-  // wave after its reduce, so every wait points to an earlier slot.
+  // Position p of the order runs on CTA p % G, in increasing p.  It is the
+  // order the library's two-shot plans use, over tmax x N tiles taken
+  // tile-major over the owners (an owner's missing last tile leaves its two
+  // positions idle), each reduced once and then copied once: the first wave reduces
+  // tiles 0 .. G-1; from the second wave on, reduce and copy positions
+  // alternate in a checkerboard of (wave p / G, CTA) until the reduces run
+  // out, and the rest are copies.  Copy k takes the k-th tile reduced; its
+  // reduce comes at least one wave earlier (from the third wave on, two), so
+  // every wait points to an earlier position.  In closed form: R, the
+  // reduces before p had the reduces never run out; p reduces tile R if it
+  // is a reduce position and R < tiles, else copies tile p - min(R, tiles).
+  const uint64_t nt = (uint64_t)a.tmax * N;
   for (uint32_t slot = c; slot < a.slots; slot += G) {
     if (threadIdx.x == 0) {
       const uint32_t w = slot / G;
-      const bool reduce = ((w + c) & 1u) == 0;
-      const uint32_t before = (reduce == ((w & 1u) == 0)) ? (c + 1) / 2 : c / 2;
-      const int64_t idx = (int64_t)w * a.half + before - (reduce ? 0 : (int64_t)a.lag);
-      const uint64_t nt = (uint64_t)a.tmax * N;
+      uint64_t R = c;
+      bool reduce_pos = true;
+      if (w > 0) {
+        R = (uint64_t)G + (uint64_t)(w - 1) * a.half + ((w & 1u) ? c / 2 : (c + 1) / 2);
+        reduce_pos = ((w + c) & 1u) == 0;
+      }
+      const bool reduce = reduce_pos && R < nt;
+      const uint64_t idx = reduce ? R : slot - (R < nt ? R : nt);
       int kind = 0;
       uint32_t o = 0;
       int64_t t = -1;
-      if (idx >= 0 && (uint64_t)idx < nt) {
-        t = idx / N;
+      if (idx < nt) {
+        t = (int64_t)(idx / N);
         o = (uint32_t)(idx % N);
         kind = reduce ? 1 : 2;
       }
@@ -337,13 +347,12 @@ extern "C" purlin_status purlin_all_reduce_noalloc(int world, const void* const*
   a.elem = (uint32_t)E;
   a.world = (uint32_t)world;
   a.tmax = (uint32_t)tmax;
-  // an even grid (the checkerboard of slots), no larger than two slots per tile
+  // an even grid (the checkerboard of positions), no larger than two positions per tile
   const uint64_t nt = tmax * (uint64_t)world;
   uint64_t g = std::min<uint64_t>((uint64_t)ctas, 2 * nt);
   g = std::max<uint64_t>(2, g & ~1ull);
   a.half = (uint32_t)(g / 2);
-  a.lag = a.half;  // copies one wave after their reduce
-  a.slots = (uint32_t)(((nt + a.lag + a.half - 1) / a.half) * g);
+  a.slots = (uint32_t)(2 * nt);
   a.dst_coaligned = same;
   const int grid = (int)g;
 

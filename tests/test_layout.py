@@ -543,3 +543,46 @@ def test_two_shot_fused_items(world):
         st, *_ = P.purlin_plan_describe(P.PL_COLL_ALL_REDUCE, world, P.PL_BF16, [1 << 20], None, None, 152,
                                         dict({"layout": P.PL_LAYOUT_TWO_SHOT_FUSED}, **bad))
         assert st == P.PL_ERR_UNSUPPORTED, bad
+
+
+def _noalloc_position(G, nt, p):
+    """Position p of the allocation-free AllReduce's order (the closed form its
+    kernel computes, csrc/noalloc.cu): (1, tile) reduce or (2, tile) copy, the
+    tiles numbered tile-major over the owners."""
+    w, c = divmod(p, G)
+    if w == 0:
+        R, reduce_pos = c, True
+    else:
+        R = G + (w - 1) * (G // 2) + (c // 2 if w % 2 else (c + 1) // 2)
+        reduce_pos = (w + c) % 2 == 0
+    if reduce_pos and R < nt:
+        return 1, R
+    return 2, p - min(R, nt)
+
+
+@pytest.mark.parametrize("world,n", [(8, 32 << 20), (8, 3_000_000), (3, 300001), (16, 4 * 65536 + 3), (2, 40)])
+def test_noalloc_order_is_the_two_shot_order(world, n):
+    """The allocation-free AllReduce computes its work positions in the kernel
+    instead of uploading a plan.  Restated here, its closed form gives the
+    layout engine's two-shot order (64 KiB tiles, the same even grid) item
+    for item.  The sizes give every owner the same number of tiles."""
+    E, T = 2, 65536
+    items, grid, _ = _describe(P.PL_COLL_ALL_REDUCE, world, P.PL_BF16, [n * E],
+                               tune={"layout": P.PL_LAYOUT_TWO_SHOT, "chunk_bytes": T})
+    q, rem = divmod(n, world)
+    start = [(o * q + min(o, rem)) * E for o in range(world + 1)]
+    tiles = {-(-(start[o + 1] - start[o]) // T) for o in range(world)}
+    assert len(tiles) == 1
+    nt = tiles.pop() * world
+    assert len(items) == 2 * nt and grid % 2 == 0
+    assert grid == max(2, min(2 * 152, 2 * nt) & ~1)   # the allocation-free call's grid
+    for p, it in enumerate(items):
+        if popcount(it["src_mask"] & 0xFFFF) > 1:
+            o = (it["dst_mask"] & 0xFFFF).bit_length() - 1
+            kind = 1
+        else:
+            o = (it["src_mask"] >> 16).bit_length() - 1
+            kind = 2
+        t = (it["src_off"] - start[o]) // T
+        assert (kind, t * world + o) == _noalloc_position(grid, nt, p), p
+        assert it["cta"] == p % grid
