@@ -561,10 +561,21 @@ __global__ void __launch_bounds__(snac_max_threads<NS>(), 2) snac_kernel(const _
         s_notify = it.notify;
         int ok = 1;
         const unsigned long long t0 = a.trace ? globaltimer() : 0ull;
-        if (it.wait) ok = consume_wait(a, a.flags + (it.wait - 1), s_epoch);
+        if constexpr (KIND == kKindRing) {
+          // every ring item but the first stages waits: the status word is
+          // loaded together with the wait's first load (one round trip to
+          // the L2 for both); a wait that spins reads it again
+          const uint32_t status = ld_volatile(&a.ctl[kCtlStatus]);
+          if (it.wait) ok = consume_wait(a, a.flags + (it.wait - 1), s_epoch);
+          if (status != 0) ok = 0;
+        } else {
+          if (it.wait) ok = consume_wait(a, a.flags + (it.wait - 1), s_epoch);
+        }
         s_t0 = t0;
         s_wait_ns = a.trace ? (uint32_t)min(globaltimer() - t0, 0xFFFFFFFFull) : 0u;
-        if (a.sync && ok && ld_volatile(&a.ctl[kCtlStatus]) != 0) ok = 0;
+        if constexpr (KIND != kKindRing) {
+          if (a.sync && ok && ld_volatile(&a.ctl[kCtlStatus]) != 0) ok = 0;
+        }
         s_ok = ok;
       }
     }
@@ -588,7 +599,10 @@ __global__ void __launch_bounds__(snac_max_threads<NS>(), 2) snac_kernel(const _
     __syncthreads();
     if (threadIdx.x == 0) {
       if (s_notify && i + 1 != a.drop_notify) {
-        __threadfence();
+        // a release is cumulative: it orders every store of the CTA that the
+        // barrier ordered before it (the ring's chain of 14 stages per tile
+        // goes without the extra full fence; the other kinds keep it)
+        if constexpr (KIND != kKindRing) __threadfence();
         st_release(a.flags + (s_notify - 1), s_epoch);
       }
       if (a.trace) trace_put(a, s_t0, globaltimer(), i, s_wait_ns, s_len);
