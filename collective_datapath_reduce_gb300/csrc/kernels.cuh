@@ -600,14 +600,17 @@ __global__ void __launch_bounds__(snac_max_threads<NS>(), 2) snac_kernel(const _
     if (threadIdx.x == 0) {
       if (s_notify && i + 1 != a.drop_notify) {
         // a release is cumulative: it orders every store of the CTA that the
-        // barrier ordered before it (the ring's chain of 14 stages per tile
-        // goes without the extra full fence; the other kinds keep it)
+        // barrier ordered before it (the ring's chains of 2 (world - 1)
+        // stages per tile go without the extra full fence; the other kinds
+        // keep it)
         if constexpr (KIND != kKindRing) __threadfence();
         st_release(a.flags + (s_notify - 1), s_epoch);
       }
       if (a.trace) trace_put(a, s_t0, globaltimer(), i, s_wait_ns, s_len);
     }
   }
+  // a loop that stopped at an error may leave the next item's copy in flight
+  if (threadIdx.x == 0) item_prefetch_wait();
   if (a.sync) {
     // (every CTA made its last queue fetch before counting itself done)
     snac_finish(a, s_epoch, a.queue != 0);
