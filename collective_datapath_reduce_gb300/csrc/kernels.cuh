@@ -490,6 +490,7 @@ __global__ void __launch_bounds__(snac_max_threads<NS>(), 2) snac_kernel(const _
   __shared__ const char* s_fsrc;  // fused items: the copied tile
   __shared__ uint32_t s_next_i, s_q_i;  // thread 0's item cursor (kept out of the registers of the Atoms)
   __shared__ __align__(16) Item s_next;  // the next item, prefetched by thread 0
+  __shared__ uint32_t s_raised;          // ring: the flag this CTA raised for its last item (0: none)
   __shared__ unsigned long long s_t0;
   grid_dep_wait();
 
@@ -508,6 +509,9 @@ __global__ void __launch_bounds__(snac_max_threads<NS>(), 2) snac_kernel(const _
     step = 1;
   }
   if (threadIdx.x == 0) s_epoch = a.sync ? ld_volatile(&a.ctl[kCtlEpoch]) + 1u : 0u;
+  if constexpr (KIND == kKindRing) {
+    if (threadIdx.x == 0) s_raised = 0u;
+  }
 
   // Thread 0 copies the next item into shared memory while the CTA moves the
   // current one (and, on the queue, fetches the index of the item after it).
@@ -562,12 +566,17 @@ __global__ void __launch_bounds__(snac_max_threads<NS>(), 2) snac_kernel(const _
         int ok = 1;
         const unsigned long long t0 = a.trace ? globaltimer() : 0ull;
         if constexpr (KIND == kKindRing) {
-          // every ring item but the first stages waits: the status word is
-          // loaded together with the wait's first load (one round trip to
-          // the L2 for both); a wait that spins reads it again
-          const uint32_t status = ld_volatile(&a.ctl[kCtlStatus]);
-          if (it.wait) ok = consume_wait(a, a.flags + (it.wait - 1), s_epoch);
-          if (status != 0) ok = 0;
+          // A tile's stages come one wave apart, so most land on the CTA that
+          // ran the stage before: a wait for the flag this CTA raised for
+          // its last item is met (its stores are ordered before this item by
+          // the block barrier).  Any other wait loads the status word with
+          // its first load (one round trip to the L2 for both); a wait that
+          // spins reads it again.
+          if (it.wait && it.wait != s_raised) {
+            const uint32_t status = ld_volatile(&a.ctl[kCtlStatus]);
+            ok = consume_wait(a, a.flags + (it.wait - 1), s_epoch);
+            if (status != 0) ok = 0;
+          }
         } else {
           if (it.wait) ok = consume_wait(a, a.flags + (it.wait - 1), s_epoch);
         }
@@ -606,6 +615,7 @@ __global__ void __launch_bounds__(snac_max_threads<NS>(), 2) snac_kernel(const _
         if constexpr (KIND != kKindRing) __threadfence();
         st_release(a.flags + (s_notify - 1), s_epoch);
       }
+      if constexpr (KIND == kKindRing) s_raised = (s_notify && i + 1 != a.drop_notify) ? s_notify : 0u;
       if (a.trace) trace_put(a, s_t0, globaltimer(), i, s_wait_ns, s_len);
     }
   }
