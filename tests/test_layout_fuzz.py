@@ -36,12 +36,13 @@ def tunes():
             "path": st.sampled_from([P.PATH_REGISTER, P.PATH_BULK]),
             "chunk_bytes": st.sampled_from([1024, 4096, 16384, 65536]),
             "stages": st.integers(2, 5),
-            "store_hint": st.sampled_from([1, 2]),
+            "store_hint": st.sampled_from([1, 2, 3]),
             "min_cta_bytes": st.sampled_from([16, 512, 4096, 65536]),
             "interleave_bytes": st.sampled_from([-1, 512, 4096, 16384]),
             "max_ctas": st.sampled_from([1, 7, 128]),
             "schedule": st.sampled_from([P.PL_SCHED_ITEM, P.PL_SCHED_STREAM, P.PL_SCHED_QUEUE,
                                          P.PL_SCHED_QUEUE_GUIDED]),
+            "snac_lag": st.sampled_from([1, 2, 3, 5, 64]),
         }))
 
 
